@@ -1,0 +1,88 @@
+"""Plants plausible mistakes in the oracle (on the CPU, through monkeypatching) and checks that at
+least one pin catches each: a pinned oracle must not survive a dropped term, a wrong sign or index,
+or a transposed operand."""
+import numpy as np
+import pytest
+
+from oracle import codebook as ocb
+from oracle import fibquant as fq
+
+import test_oracle_codebook as tc
+import test_oracle_encode as te
+
+
+def _fails(fn, *args):
+    try:
+        fn(*args)
+    except (AssertionError, ValueError, IndexError):
+        return True
+    return False
+
+
+def test_transposed_rotation_is_caught(monkeypatch):
+    orig = fq.rotate_normalise
+    monkeypatch.setattr(fq, "rotate_normalise", lambda x, Pi, nu: orig(x, np.asarray(Pi).T, nu))
+    assert _fails(te.test_decode_encode_round_trip_on_codeword_vectors, 64, 4, 256)
+
+
+def test_transposed_inverse_rotation_is_caught(monkeypatch):
+    def bad(nu, idx, C, Pi):
+        M, nb = idx.shape
+        y = np.asarray(C)[idx].reshape(M, -1)
+        return np.asarray(nu)[:, None] * (y @ np.asarray(Pi).T)
+    monkeypatch.setattr(fq, "decode", bad)
+    assert _fails(te.test_decode_encode_round_trip_on_codeword_vectors, 64, 2, 16)
+
+
+def test_dropped_norm_is_caught(monkeypatch):
+    monkeypatch.setattr(fq, "row_norms", lambda x: np.ones(np.asarray(x).shape[0]))
+    assert _fails(te.test_norm_against_library_and_closed_form)
+    assert _fails(te.test_decode_encode_round_trip_on_codeword_vectors, 64, 4, 256)
+
+
+def test_expanded_form_without_norm_term_is_caught(monkeypatch):
+    def bad(P, C, chunk_elems=0):
+        return np.argmin(-2.0 * np.asarray(P) @ np.asarray(C).T, axis=1)
+    monkeypatch.setattr(fq, "nearest_codeword", bad)
+    assert _fails(te.test_nearest_codeword_matches_kdtree)
+
+
+def test_wrong_tie_break_is_caught(monkeypatch):
+    def bad(P, C, chunk_elems=0):
+        d2 = np.sum((np.asarray(P)[:, None, :] - np.asarray(C)[None]) ** 2, axis=2)
+        return d2.shape[1] - 1 - np.argmin(d2[:, ::-1], axis=1)
+    monkeypatch.setattr(fq, "nearest_codeword", bad)
+    assert _fails(te.test_codewords_map_to_themselves_and_ties_go_low)
+
+
+def test_msb_first_packing_is_caught(monkeypatch):
+    orig = fq.pack
+    def bad(idx, B):
+        idx = np.asarray(idx)
+        rev = np.zeros_like(idx)
+        for t in range(B):
+            rev |= ((idx >> t) & 1) << (B - 1 - t)
+        return orig(rev, B)
+    monkeypatch.setattr(fq, "pack", bad)
+    for B, idx, want in te._golden_pack_vectors():
+        if _fails(te.test_pack_golden, B, idx, want):
+            return
+    pytest.fail("MSB-first packing survived the golden vectors")
+
+
+def test_missing_sign_fix_is_caught(monkeypatch):
+    monkeypatch.setattr(ocb, "haar_rotation", lambda G: np.linalg.qr(np.asarray(G))[0])
+    assert _fails(tc.test_haar_rotation_law)
+
+
+def test_shifted_radius_quantile_is_caught(monkeypatch):
+    def bad(d, k, N):
+        p = (np.arange(N) + 1.0) / (N + 1)
+        return np.sqrt(1.0 - (1.0 - p) ** (4.0 / d))
+    monkeypatch.setattr(ocb, "companded_radii", bad)
+    assert _fails(tc.test_k2_radii_closed_form_matches_beta_quantile)
+
+
+def test_wrong_source_law_is_caught(monkeypatch):
+    monkeypatch.setattr(ocb, "source_points", lambda g, k: np.asarray(g)[:, :k] / np.sqrt(np.asarray(g).shape[1]))
+    assert _fails(tc.test_source_points_law)

@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Throughput of the FibQuant codec hot path on one GB300 (or N independent replicas).
+
+One step = the whole hot path over one batch of the GPT-2-small-shaped KV workload
+(12 layers x 12 heads x 1024 tokens, d = 64, k = 2, N = 256, b = 4 bits per coordinate):
+encode all of K and all of V (2 x 147,456 vectors: norm, rotation, nearest codeword, fixed-
+address packing), then random-access decode of 65,536 uniformly drawn rows from each
+(gather, unpack, codeword lookup, inverse rotation, scaling). Inputs are resident in HBM when
+the timed region starts; L2 is flushed (a 256 MB write) before every timed step, outside the
+step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it.
+
+`--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
+sample of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "KV vectors/s encoded and decoded (fp16 GB/s) per bitrate; % of HBM/TC roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources: ties a committed ncu traffic figure to the kernels it measured."""
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "random_access_kv_gb300", "csrc")
+    for name in sorted(os.listdir(cdir)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(cdir, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: int):
+    """dram bytes per launch from profiles/<kernel>_w<workload>.md if it was taken on these sources."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_w{workload}.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch")):
+                k, v = line.split(":", 1)
+                vals[k.strip().lstrip("- ")] = v.strip().strip("`")
+    if vals.get("source_hash") != source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def workload_bytes(w, R: int) -> tuple[int, int]:
+    """Algorithmic HBM bytes per encoded row and per gathered row."""
+    enc = 2 * w.d + 4 + R / 8                # read x fp16, write nu fp32 and the R-bit record
+    gat = 8 + 4 + R / 8 + 2 * w.d            # read idx int64, nu, record; write x_hat fp16
+    return enc, gat
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline leg): the fp64 oracle as it stands.
+
+def oracle_sample_rows(cfg: int) -> tuple[int, int]:
+    """Rows per tensor encoded and rows gathered per tensor in one bounded oracle step."""
+    return {2: (8192, 4096)}.get(cfg, (2048, 1024))
+
+
+def time_oracle(cfg: int, steps: int) -> dict:
+    from oracle import fibquant as ofq
+    from oracle import workloads as ow
+    w = synth.WORKLOADS[cfg]
+    C, Pi = ow.codebook(cfg), ow.rotation(cfg)
+    enc_rows, gat_rows = oracle_sample_rows(cfg)
+    xs = [synth.kv_tensor(cfg, t, rows=enc_rows) for t in range(w.tensors)]
+    sels = [synth.gather_indices(cfg, t, enc_rows, gat_rows) for t in range(w.tensors)]
+    vecs = 0
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for x, sel in zip(xs, sels):
+            nu, idx = ofq.encode(x, C, Pi)
+            words = ofq.pack(idx, w.B)
+            back = ofq.unpack(words, enc_rows, w.d // w.k, w.B)
+            ofq.decode(nu[sel], back[sel], C, Pi).astype(np.float16)
+            vecs += enc_rows + gat_rows
+    dt = time.perf_counter() - t0
+    return {"value": vecs / dt, "seconds": dt, "vectors": vecs,
+            "sample": f"{w.tensors} x ({enc_rows} rows encoded + packed, {gat_rows} gathered + decoded) per step "
+                      f"of workload {cfg}, {steps} steps, numpy fp64"}
+
+
+def run_reference(args) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = synth.WORKLOADS[args.workload]
+    time_oracle(args.workload, max(1, args.warmup))
+    r = time_oracle(args.workload, args.steps)
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "vectors/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r["seconds"] / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": r["sample"]},
+        "cpu_baseline": {"value": r["value"], "unit": "vectors/s", "cores": cores, "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": "vectors/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm.
+
+def run_ours(args) -> None:
+    import torch
+    import random_access_kv_gb300 as fq
+    from random_access_kv_gb300 import build as fbuild
+    from random_access_kv_gb300 import codebook as pcb
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    cfg = args.workload
+    w = synth.WORKLOADS[cfg]
+    if w.op != "encode+gather":
+        raise SystemExit("bench times the encode + random-access decode workload (2)")
+    C, Pi = pcb.for_workload(cfg)
+    ctx = fq.fq_codebook_load(C, Pi, local)
+    R = fq.fq_record_bits(ctx)
+    M, G, d = w.rows, w.gather, w.d
+    x_host = [torch.from_numpy(synth.kv_tensor(cfg, t)).pin_memory() for t in range(w.tensors)]
+    i_host = [torch.from_numpy(synth.gather_indices(cfg, t, M, G)).pin_memory() for t in range(w.tensors)]
+    xs = [h.to(dev) for h in x_host]
+    idxs = [h.to(dev) for h in i_host]
+    stores = [fq.alloc_store(ctx, M, dev) for _ in range(w.tensors)]
+    outs = [torch.empty((G, d), dtype=torch.float16, device=dev) for _ in range(w.tensors)]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step(ev=None):
+        for t in range(w.tensors):
+            nu, codes = stores[t]
+            if ev is not None:
+                ev[f"enc{t}"][0].record(stream)
+            fq.fq_encode(ctx, xs[t], M, nu, codes, 0, sp)
+            if ev is not None:
+                ev[f"enc{t}"][1].record(stream)
+        for t in range(w.tensors):
+            nu, codes = stores[t]
+            if ev is not None:
+                ev[f"gat{t}"][0].record(stream)
+            fq.fq_decode_gather(ctx, nu, codes, M, idxs[t], G, outs[t], sp)
+            if ev is not None:
+                ev[f"gat{t}"][1].record(stream)
+
+    launches_per_step = 2 * w.tensors
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fq.fq_status(ctx, sp) != 0:
+        raise SystemExit("device flags set during warm-up")
+
+    names = [f"enc{t}" for t in range(w.tensors)] + [f"gat{t}" for t in range(w.tensors)]
+    per_step = []
+    kern = {n: [] for n in names}
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        step(ev)
+        s1.record(stream)
+        per_step.append((s0, s1, ev))
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b, _ in per_step]
+    for _, _, ev in per_step:
+        for n in names:
+            kern[n].append(ev[n][0].elapsed_time(ev[n][1]))
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flags = fq.fq_status(ctx, sp)
+
+    vec_per_step = w.tensors * (M + G)
+    value = world * vec_per_step * args.steps / (total_ms / 1e3)
+
+    # End to end through the public API from pinned host memory: H2D of the inputs, encode,
+    # gather, D2H of the codes, norms and decoded rows, every step.
+    nu_host = [torch.empty(M, dtype=torch.float32).pin_memory() for _ in range(w.tensors)]
+    code_host = [torch.empty_like(stores[t][1], device="cpu").pin_memory() for t in range(w.tensors)]
+    out_host = [torch.empty((G, d), dtype=torch.float16).pin_memory() for _ in range(w.tensors)]
+
+    def e2e_step():
+        for t in range(w.tensors):
+            xs[t].copy_(x_host[t], non_blocking=True)
+            idxs[t].copy_(i_host[t], non_blocking=True)
+        step()
+        for t in range(w.tensors):
+            nu_host[t].copy_(stores[t][0], non_blocking=True)
+            code_host[t].copy_(stores[t][1], non_blocking=True)
+            out_host[t].copy_(outs[t], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    h2d = sum(x.numel() * 2 + i.numel() * 8 for x, i in zip(x_host, i_host))
+    d2h = sum(n.numel() * 4 + c.numel() * 4 + o.numel() * 2 for n, c, o in zip(nu_host, code_host, out_host))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * vec_per_step * args.steps / (e2e_total / 1e3)
+
+    enc_b, gat_b = workload_bytes(w, R)
+    enc_ms = statistics.mean(kern["enc0"] + kern.get("enc1", []))
+    gat_ms = statistics.mean(kern["gat0"] + kern.get("gat1", []))
+    peaks = measured_peaks()
+    if enc_ms * M >= gat_ms * G:
+        dom, dom_bytes, dom_ms, kname = "encode", enc_b * M, enc_ms, "fq_encode"
+    else:
+        dom, dom_bytes, dom_ms, kname = "decode_gather", gat_b * G, gat_ms, "fq_decode_gather"
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": int(dom_bytes), "launch_ms": round(dom_ms, 5),
+                "encode_launch_ms": round(enc_ms, 5), "gather_launch_ms": round(gat_ms, 5),
+                "encode_gbs": round(enc_b * M / (enc_ms / 1e3) / 1e9, 1),
+                "gather_gbs": round(gat_b * G / (gat_ms / 1e3) / 1e9, 1)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle(cfg, args.cpu_steps)
+        cpu = {"value": r["value"], "unit": "vectors/s", "cores": host_cores(), "kind": "oracle",
+               "sample": r["sample"], "seconds": round(r["seconds"], 2)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "vectors/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "rows_per_tensor": M, "tensors": w.tensors, "d": d, "k": w.k,
+                       "N": w.N, "bits_per_coordinate": w.B / w.k, "record_bits": R, "gather_per_tensor": G,
+                       "l2": "flushed before every timed step (256 MB write, outside the step events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "fp16_gbps": value * 2 * d / 1e9,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "vectors/s", "h2d_bytes_per_step": int(h2d),
+                    "d2h_bytes_per_step": int(d2h)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "device_flags": flags,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+"""ctypes binding of libfq.so: the C ABI of include/fq.h under the same names.
+
+Argument marshalling only: every function takes device buffers as torch CUDA tensors (or raw
+integer addresses), passes their addresses and sizes to the C entry point of the same name and
+raises ``FQError`` on a non-zero return code. No step of the codec runs here.
+
+The library is loaded from this package directory. If it is missing the import fails loudly
+(``FQLibraryMissing``): there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfq.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "fq.h")
+
+FQ_OK, FQ_EINVAL, FQ_ENOMEM, FQ_ECUDA, FQ_EALIGN, FQ_ENODEV = range(6)
+FQ_FLAG_RANGE, FQ_FLAG_NONFINITE, FQ_FLAG_TIMEOUT = 1, 2, 4
+
+
+class FQLibraryMissing(ImportError):
+    pass
+
+
+class FQError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {strerror(code)} ({code})")
+
+
+_c_void_p, _i64, _int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+
+_SIGNATURES = {
+    "fq_codebook_load": (_int, [ctypes.POINTER(_c_void_p), _c_void_p, _int, _int, _c_void_p, _int, _int]),
+    "fq_encode": (_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p, _i64, _c_void_p]),
+    "fq_encode_append": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "fq_decode": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fq_decode_gather": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fq_decode_gather_f32": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fq_code_words": (_i64, [_c_void_p, _i64]),
+    "fq_record_bits": (_int, [_c_void_p]),
+    "fq_shape": (_int, [_c_void_p, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+    "fq_status": (_int, [_c_void_p, _c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "fq_destroy": (None, [_c_void_p]),
+    "fq_strerror": (ctypes.c_char_p, [_int]),
+}
+
+_lib = None
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions declared in include/fq.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fq_[a-z0-9_]+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded on first use)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FQLibraryMissing(f"{LIB_PATH} is not built; run random_access_kv_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return lib().fq_strerror(int(code)).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if hasattr(t, "data_ptr"):
+        return t.data_ptr() if t.numel() else None
+    if hasattr(t, "ctypes"):            # numpy host array
+        return t.ctypes.data
+    raise TypeError(f"cannot take the address of {type(t)}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != FQ_OK:
+        raise FQError(fn, rc)
+
+
+class Context:
+    """Owns an ``fq_ctx*``; frees it with ``fq_destroy`` on ``close()`` or garbage collection."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    @property
+    def _as_parameter_(self):
+        return ctypes.c_void_p(self.handle)
+
+    def close(self) -> None:
+        if self.handle:
+            lib().fq_destroy(ctypes.c_void_p(self.handle))
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def fq_codebook_load(C, Pi, device: int = 0) -> Context:
+    """C: float32 [N, k] host array; Pi: float32 [d, d] host array (C-contiguous numpy)."""
+    import numpy as np
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    Pi = np.ascontiguousarray(Pi, dtype=np.float32)
+    if C.ndim != 2 or Pi.ndim != 2 or Pi.shape[0] != Pi.shape[1]:
+        raise ValueError("C must be [N, k] and Pi [d, d]")
+    h = _c_void_p()
+    rc = lib().fq_codebook_load(ctypes.byref(h), C.ctypes.data, C.shape[0], C.shape[1],
+                                Pi.ctypes.data, Pi.shape[0], int(device))
+    _check("fq_codebook_load", rc)
+    return Context(h.value)
+
+
+def fq_encode(ctx: Context, x, M: int, nu, codes, row0: int = 0, stream=None) -> None:
+    _check("fq_encode", lib().fq_encode(ctx, _ptr(x), int(M), _ptr(nu), _ptr(codes), int(row0),
+                                        _stream(stream)))
+
+
+def fq_encode_append(ctx: Context, x, n_seq: int, n_new: int, seq_capacity: int, t0: int, nu, codes,
+                     stream=None) -> None:
+    _check("fq_encode_append", lib().fq_encode_append(ctx, _ptr(x), int(n_seq), int(n_new),
+                                                      int(seq_capacity), int(t0), _ptr(nu), _ptr(codes),
+                                                      _stream(stream)))
+
+
+def fq_decode(ctx: Context, nu, codes, M: int, out, stream=None) -> None:
+    _check("fq_decode", lib().fq_decode(ctx, _ptr(nu), _ptr(codes), int(M), _ptr(out), _stream(stream)))
+
+
+def fq_decode_gather(ctx: Context, nu, codes, M: int, idx, n: int, out, stream=None) -> None:
+    _check("fq_decode_gather", lib().fq_decode_gather(ctx, _ptr(nu), _ptr(codes), int(M), _ptr(idx), int(n),
+                                                      _ptr(out), _stream(stream)))
+
+
+def fq_decode_gather_f32(ctx: Context, nu, codes, M: int, idx, n: int, out, stream=None) -> None:
+    _check("fq_decode_gather_f32", lib().fq_decode_gather_f32(ctx, _ptr(nu), _ptr(codes), int(M), _ptr(idx),
+                                                              int(n), _ptr(out), _stream(stream)))
+
+
+def fq_code_words(ctx: Context, M: int) -> int:
+    w = lib().fq_code_words(ctx, int(M))
+    if w < 0:
+        raise FQError("fq_code_words", FQ_EINVAL)
+    return int(w)
+
+
+def fq_record_bits(ctx: Context) -> int:
+    return int(lib().fq_record_bits(ctx))
+
+
+def fq_shape(ctx: Context) -> tuple[int, int, int]:
+    d, k, N = _int(), _int(), _int()
+    _check("fq_shape", lib().fq_shape(ctx, ctypes.byref(d), ctypes.byref(k), ctypes.byref(N)))
+    return d.value, k.value, N.value
+
+
+def fq_status(ctx: Context, stream=None) -> int:
+    f = ctypes.c_uint32()
+    _check("fq_status", lib().fq_status(ctx, _stream(stream), ctypes.byref(f)))
+    return int(f.value)
+
+
+def fq_destroy(ctx: Context) -> None:
+    ctx.close()
+
+
+def fq_strerror(code: int) -> str:
+    return strerror(code)

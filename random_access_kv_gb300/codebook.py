@@ -1,0 +1,124 @@
+"""Host-side builder of the shared FibQuant rotation and codebook (offline, numpy/scipy).
+
+The codec's kernels take the codebook C [N, k] and rotation Pi [d, d] as inputs; this module makes
+them from seeded random draws, following [FibQuant §2.1, §2.2] of the page "FibQuant: universal
+vector quantisation for random-access KV-cache compression":
+
+  rotation  Pi = Q diag(sign(diag R)) for G = Q R, G a d x d standard Gaussian (Haar law).
+  radii     Bennett-Gersho companding of the spherical-Beta block law: the point density
+            ~ f^(k/(k+2)) makes t = rho^2 of the codewords Beta(k/2, 1 + k(d-k-2)/(2(k+2)));
+            r_n is the square root of that law's quantile at (n + 1/2)/N.
+  angles    k = 2: Fibonacci spiral (golden angle per index). k >= 3: Roberts-Kronecker points
+            frac(s + (n+1) phi_k^-j), j = 1..k, pushed through the inverse normal CDF and
+            normalised; phi_k solves x^(k+1) = x + 1. k = d: the unit directions alone.
+  Lloyd     multi-restart Lloyd on draws of the block source (first k coordinates of a Gaussian
+            vector over its norm); restart r >= 1 rotates the start by a k x k Haar matrix; the
+            lowest training MSE wins.
+
+This is construction-time code, not part of the encode/decode path.
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy import special
+
+
+def haar(G: np.ndarray) -> np.ndarray:
+    Q, R = np.linalg.qr(np.asarray(G, dtype=np.float64))
+    d = np.diag(R)
+    return Q * np.where(d < 0, -1.0, 1.0)
+
+
+def radii(d: int, k: int, N: int) -> np.ndarray:
+    alpha = 0.5 * k
+    beta = 1.0 + k * (d - k - 2) / (2.0 * (k + 2))
+    q = (np.arange(N, dtype=np.float64) + 0.5) / N
+    return np.sqrt(special.betaincinv(alpha, beta, q))
+
+
+def _roberts_phi(k: int) -> float:
+    x = 2.0
+    for _ in range(100):                    # Newton on x^(k+1) - x - 1, from above the root
+        x -= (x ** (k + 1) - x - 1.0) / ((k + 1) * x ** k - 1.0)
+    return x
+
+
+def directions(N: int, k: int, s: float) -> np.ndarray:
+    if k == 2:
+        golden = np.pi * (3.0 - np.sqrt(5.0))
+        a = golden * np.arange(N)
+        return np.column_stack([np.cos(a), np.sin(a)])
+    g = _roberts_phi(k)
+    steps = np.power(g, -np.arange(1.0, k + 1.0))
+    pts = np.modf(s + np.outer(np.arange(1, N + 1, dtype=np.float64), steps))[0]
+    z = special.ndtri(pts)
+    return z / np.linalg.norm(z, axis=1, keepdims=True)
+
+
+def initial(kind: str, d: int, k: int, N: int, s: float = 0.5) -> np.ndarray:
+    u = directions(N, k, s)
+    if kind == "sphere":
+        return u
+    return radii(d, k, N)[:, None] * u
+
+
+def block_source(g: np.ndarray, k: int) -> np.ndarray:
+    g = np.asarray(g, dtype=np.float64)
+    return g[:, :k] / np.linalg.norm(g, axis=1, keepdims=True)
+
+
+def _nearest(Y: np.ndarray, C: np.ndarray) -> tuple[np.ndarray, float]:
+    n2 = np.einsum("ij,ij->i", C, C)
+    idx = np.empty(len(Y), dtype=np.int64)
+    err = 0.0
+    rows = max(1, 8_000_000 // len(C))
+    for a in range(0, len(Y), rows):
+        y = Y[a:a + rows]
+        score = y @ (-2.0 * C.T)
+        score += n2
+        i = score.argmin(axis=1)
+        idx[a:a + rows] = i
+        err += float(np.sum((y - C[i]) ** 2))
+    return idx, err / len(Y)
+
+
+def refine(C: np.ndarray, Y: np.ndarray, iters: int, rtol: float = 1e-6) -> tuple[np.ndarray, float]:
+    C = C.copy()
+    idx, mse = _nearest(Y, C)
+    for _ in range(iters):
+        cnt = np.bincount(idx, minlength=len(C)).astype(np.float64)
+        tot = np.zeros_like(C)
+        for j in range(C.shape[1]):
+            tot[:, j] = np.bincount(idx, weights=Y[:, j], minlength=len(C))
+        live = cnt > 0
+        C[live] = tot[live] / cnt[live, None]
+        idx, new = _nearest(Y, C)
+        done = mse - new <= rtol * mse
+        mse = new
+        if done:
+            break
+    return C, mse
+
+
+def build(kind: str, d: int, k: int, N: int, train_gaussians: np.ndarray, iters: int,
+          restart_gaussians=(), s: float = 0.5) -> tuple[np.ndarray, float]:
+    """(C fp64 [N, k], training MSE)."""
+    Y = block_source(train_gaussians, k)
+    C0 = initial(kind, d, k, N, s)
+    best = refine(C0, Y, iters)
+    for G in restart_gaussians:
+        cand = refine(C0 @ haar(G).T, Y, iters)
+        if cand[1] < best[1]:
+            best = cand
+    return best
+
+
+def for_workload(cfg: int) -> tuple[np.ndarray, np.ndarray]:
+    """(C float32 [N, k], Pi float32 [d, d]) of one of the synthetic workloads."""
+    import synth
+    w = synth.WORKLOADS[cfg]
+    Pi = haar(synth.rotation_gaussian(cfg, w.d)).astype(np.float32)
+    C, _ = build(w.codebook_kind, w.d, w.k, w.N, synth.source_gaussians(cfg, w.lloyd_train, w.d),
+                 w.lloyd_iters, [synth.restart_gaussian(cfg, w.k, r) for r in range(1, w.lloyd_restarts)],
+                 synth.kronecker_offset(cfg))
+    return C.astype(np.float32), Pi

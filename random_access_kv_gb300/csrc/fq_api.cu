@@ -1,0 +1,248 @@
+// C ABI of libfq.so: argument validation, context set-up (derived tables built on the host in
+// double precision), kernel dispatch. Declarations and contracts are in include/fq.h.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <vector>
+
+#include "fq_internal.h"
+
+namespace {
+
+// Restores the calling thread's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) {
+            err = cudaSetDevice(dev);
+            changed = err == cudaSuccess;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int log2_exact(int N) {
+    if (N < 2 || (N & (N - 1))) return -1;
+    int b = 0;
+    while ((1 << b) < N) ++b;
+    return b;
+}
+
+void free_ctx(fq_ctx *c) {
+    if (!c) return;
+    cudaFree(c->C);
+    cudaFree(c->cc);
+    cudaFree(c->Pi);
+    cudaFree(c->Crot);
+    cudaFree(c->flags);
+    free(c);
+}
+
+template <typename T>
+cudaError_t upload(T **dst, const std::vector<T> &src) {
+    cudaError_t e = cudaMalloc((void **)dst, src.size() * sizeof(T));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice);
+}
+
+bool is_full(const fq_ctx *c) { return c->k == c->d; }
+
+}  // namespace
+
+extern "C" {
+
+const char *fq_strerror(int err) {
+    switch (err) {
+        case FQ_OK: return "ok";
+        case FQ_EINVAL: return "invalid argument";
+        case FQ_ENOMEM: return "out of memory";
+        case FQ_ECUDA: return "CUDA error";
+        case FQ_EALIGN: return "misaligned buffer";
+        case FQ_ENODEV: return "no usable sm_103 device";
+        default: return "unknown error";
+    }
+}
+
+int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const float *Pi_host, int d,
+                     int device) {
+    if (!out) return FQ_EINVAL;
+    *out = nullptr;
+    if (!C_host || !Pi_host) return FQ_EINVAL;
+    const int B = log2_exact(N);
+    if (B < 0 || N > 65536) return FQ_EINVAL;
+    const bool blocks_ok = (d == 64 || d == 128) && (k == 1 || k == 2 || k == 4 || k == 8) &&
+                           (size_t)N * k <= 32768;
+    const bool full_ok = (d == 64 && k == 64 && N >= 64);
+    if (!blocks_ok && !full_ok) return FQ_EINVAL;
+    for (size_t i = 0; i < (size_t)N * k; ++i)
+        if (!isfinite(C_host[i])) return FQ_EINVAL;
+    for (size_t i = 0; i < (size_t)d * d; ++i)
+        if (!isfinite(Pi_host[i])) return FQ_EINVAL;
+
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return FQ_ENODEV;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return FQ_ENODEV;
+    if (prop.major != 10 || prop.minor != 3) return FQ_ENODEV;
+    DeviceGuard g(device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+
+    fq_ctx *c = (fq_ctx *)calloc(1, sizeof(fq_ctx));
+    if (!c) return FQ_ENOMEM;
+    c->device = device;
+    c->d = d;
+    c->k = k;
+    c->N = N;
+    c->B = B;
+    c->nb = d / k;
+    c->R = c->nb * B;
+
+    std::vector<float> C(C_host, C_host + (size_t)N * k);
+    std::vector<float> P(Pi_host, Pi_host + (size_t)d * d);
+    std::vector<float> cc(N);
+    for (int n = 0; n < N; ++n) {
+        double s = 0;
+        for (int t = 0; t < k; ++t) s += (double)C[(size_t)n * k + t] * C[(size_t)n * k + t];
+        cc[n] = (float)s;
+    }
+    cudaError_t e = upload(&c->C, C);
+    if (e == cudaSuccess) e = upload(&c->cc, cc);
+    if (e == cudaSuccess) e = upload(&c->Pi, P);
+    if (e == cudaSuccess && is_full(c)) {
+        // Crot[n][i] = sum_j C[n][j] Pi[j][i]  (row n = Pi^T c_n), accumulated in double.
+        std::vector<float> R((size_t)N * d);
+        std::vector<double> acc(d);
+        for (int n = 0; n < N; ++n) {
+            for (int i = 0; i < d; ++i) acc[i] = 0.0;
+            for (int j = 0; j < d; ++j) {
+                const double cj = C[(size_t)n * d + j];
+                const float *prow = &P[(size_t)j * d];
+                for (int i = 0; i < d; ++i) acc[i] += cj * (double)prow[i];
+            }
+            for (int i = 0; i < d; ++i) R[(size_t)n * d + i] = (float)acc[i];
+        }
+        e = upload(&c->Crot, R);
+    }
+    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = is_full(c) ? fq::prepare_full(c) : fq::prepare_encode_blocks(c);
+    if (e == cudaSuccess && !is_full(c)) e = fq::prepare_decode_blocks(c);
+    if (e != cudaSuccess) {
+        const int rc = (e == cudaErrorMemoryAllocation) ? FQ_ENOMEM : FQ_ECUDA;
+        free_ctx(c);
+        return rc;
+    }
+    *out = c;
+    return FQ_OK;
+}
+
+int64_t fq_code_words(const fq_ctx *ctx, int64_t M) {
+    if (!ctx || M < 0 || M > (INT64_MAX - 31) / ctx->R) return -1;
+    return (M * ctx->R + 31) / 32;
+}
+
+int fq_record_bits(const fq_ctx *ctx) { return ctx ? ctx->R : -1; }
+
+int fq_shape(const fq_ctx *ctx, int *d, int *k, int *N) {
+    if (!ctx) return FQ_EINVAL;
+    if (d) *d = ctx->d;
+    if (k) *k = ctx->k;
+    if (N) *N = ctx->N;
+    return FQ_OK;
+}
+
+static int encode_common(fq_ctx *ctx, const void *x, int64_t M, fq::RowMap map, int64_t rows_total,
+                         float *nu, uint32_t *codes, void *stream) {
+    if (!ctx || M < 0) return FQ_EINVAL;
+    if (M == 0) return FQ_OK;
+    if (!x || !nu || !codes) return FQ_EINVAL;
+    if (!aligned(x, 16) || !aligned(nu, 4) || !aligned(codes, 4)) return FQ_EALIGN;
+    if (rows_total < 0 || fq_code_words(ctx, rows_total) < 0) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = is_full(ctx) ? fq::launch_encode_full(ctx, (const __half *)x, M, map, nu, codes, s)
+                                 : fq::launch_encode_blocks(ctx, (const __half *)x, M, map, nu, codes, s);
+    return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
+int fq_encode(fq_ctx *ctx, const void *x, int64_t M, float *nu, uint32_t *codes, int64_t row0,
+              void *stream) {
+    if (row0 < 0 || M > INT64_MAX - row0) return FQ_EINVAL;
+    fq::RowMap map{M > 0 ? M : 1, 0, row0};
+    return encode_common(ctx, x, M, map, row0 + M, nu, codes, stream);
+}
+
+int fq_encode_append(fq_ctx *ctx, const void *x, int64_t n_seq, int64_t n_new, int64_t seq_capacity,
+                     int64_t t0, float *nu, uint32_t *codes, void *stream) {
+    if (n_seq < 0 || n_new < 0 || t0 < 0 || seq_capacity < 0) return FQ_EINVAL;
+    if (n_new > seq_capacity || t0 > seq_capacity - n_new) return FQ_EINVAL;
+    if (n_seq > 0 && seq_capacity > INT64_MAX / n_seq) return FQ_EINVAL;
+    if (n_seq > 0 && n_new > INT64_MAX / n_seq) return FQ_EINVAL;
+    const int64_t M = n_seq * n_new;
+    fq::RowMap map{n_new > 0 ? n_new : 1, seq_capacity, t0};
+    return encode_common(ctx, x, M, map, n_seq * seq_capacity, nu, codes, stream);
+}
+
+static int decode_common(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
+                         const int64_t *idx, int64_t n, void *out, bool out_f32, void *stream) {
+    if (!ctx || M < 0 || n < 0) return FQ_EINVAL;
+    if (n == 0) return FQ_OK;
+    if (!out || (!idx && n > M)) return FQ_EINVAL;
+    if (M > 0 && (!nu || !codes)) return FQ_EINVAL;
+    if (fq_code_words(ctx, M) < 0) return FQ_EINVAL;
+    if (!aligned(out, 16) || !aligned(nu, 4) || !aligned(codes, 4) || !aligned(idx, 8)) return FQ_EALIGN;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = is_full(ctx) ? fq::launch_decode_full(ctx, nu, codes, M, idx, n, out, out_f32, s)
+                                 : fq::launch_decode_blocks(ctx, nu, codes, M, idx, n, out, out_f32, s);
+    return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
+int fq_decode(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, void *out, void *stream) {
+    return decode_common(ctx, nu, codes, M, nullptr, M, out, false, stream);
+}
+
+int fq_decode_gather(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, const int64_t *idx,
+                     int64_t n, void *out, void *stream) {
+    if (n > 0 && !idx) return FQ_EINVAL;
+    return decode_common(ctx, nu, codes, M, idx, n, out, false, stream);
+}
+
+int fq_decode_gather_f32(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
+                         const int64_t *idx, int64_t n, float *out, void *stream) {
+    if (n > 0 && !idx) return FQ_EINVAL;
+    return decode_common(ctx, nu, codes, M, idx, n, out, true, stream);
+}
+
+int fq_status(fq_ctx *ctx, void *stream, uint32_t *flags) {
+    if (!ctx || !flags) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, ctx->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flags, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return FQ_ECUDA;
+    *flags = h;
+    return FQ_OK;
+}
+
+void fq_destroy(fq_ctx *ctx) {
+    if (!ctx) return;
+    DeviceGuard g(ctx->device);
+    cudaDeviceSynchronize();
+    free_ctx(ctx);
+}
+
+}  // extern "C"

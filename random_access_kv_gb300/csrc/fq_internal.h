@@ -1,0 +1,50 @@
+// Internal declarations shared by the translation units of libfq.so.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fq.h"
+
+struct fq_ctx {
+    int device;
+    int d, k, N, B, nb, R;      // nb = d / k blocks, B = log2 N, R = nb * B
+    float *C;                    // [N x k] codebook
+    float *cc;                   // [N] |c_n|^2
+    float *Pi;                   // [d x d] rotation, row-major
+    float *Crot;                 // k == d: [N x d] rotated codebook C Pi (row n = Pi^T c_n)
+    uint32_t *flags;             // sticky FQ_FLAG_* word
+};
+
+namespace fq {
+
+// Mapping from an input row r to its store row: (r / n_new) * seq_cap + row_base + r % n_new.
+// fq_encode uses n_new = M (one sequence) and row_base = row0.
+struct RowMap {
+    int64_t n_new;
+    int64_t seq_cap;
+    int64_t row_base;
+    __host__ __device__ __forceinline__ int64_t operator()(int64_t r) const {
+        int64_t s = r / n_new;
+        return s * seq_cap + row_base + (r - s * n_new);
+    }
+};
+
+// Kernel launchers (defined in the .cu files). Each returns a cudaError_t from the launch.
+cudaError_t launch_encode_blocks(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
+                                 float *nu, uint32_t *codes, cudaStream_t s);
+cudaError_t launch_decode_blocks(const fq_ctx *ctx, const float *nu, const uint32_t *codes,
+                                 int64_t M, const int64_t *idx, int64_t n, void *out,
+                                 bool out_f32, cudaStream_t s);
+cudaError_t launch_encode_full(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
+                               float *nu, uint32_t *codes, cudaStream_t s);
+cudaError_t launch_decode_full(const fq_ctx *ctx, const float *nu, const uint32_t *codes,
+                               int64_t M, const int64_t *idx, int64_t n, void *out,
+                               bool out_f32, cudaStream_t s);
+// One-time kernel attribute set-up (dynamic shared memory limits); called by fq_codebook_load.
+cudaError_t prepare_encode_blocks(const fq_ctx *ctx);
+cudaError_t prepare_decode_blocks(const fq_ctx *ctx);
+cudaError_t prepare_full(const fq_ctx *ctx);
+
+}  // namespace fq

@@ -1,0 +1,67 @@
+"""The C ABI without a GPU: the library builds, loads and exports every function the header
+declares; host-side argument checks answer before any device work."""
+import ctypes
+
+import numpy as np
+import pytest
+
+from random_access_kv_gb300 import _binding as fb
+from random_access_kv_gb300 import build as fbuild
+
+
+@pytest.fixture(scope="module")
+def L():
+    fbuild.build()
+    return fb.lib()
+
+
+def test_exports_every_header_symbol(L):
+    names = fb.header_symbols()
+    assert "fq_encode" in names and "fq_decode_gather" in names and "fq_codebook_load" in names
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(fb._SIGNATURES)
+
+
+def test_strerror_and_null_context(L):
+    assert fb.strerror(0) == "ok"
+    assert "invalid" in fb.strerror(1)
+    assert L.fq_code_words(None, 10) == -1
+    assert L.fq_record_bits(None) == -1
+    assert L.fq_encode(None, None, 5, None, None, 0, None) == fb.FQ_EINVAL
+    assert L.fq_decode_gather(None, None, None, 5, None, 5, None, None) == fb.FQ_EINVAL
+    assert L.fq_shape(None, None, None, None) == fb.FQ_EINVAL
+    L.fq_destroy(None)
+
+
+def _load(L, C, Pi):
+    h = ctypes.c_void_p()
+    C = np.ascontiguousarray(C, dtype=np.float32)
+    Pi = np.ascontiguousarray(Pi, dtype=np.float32)
+    rc = L.fq_codebook_load(ctypes.byref(h), C.ctypes.data, C.shape[0], C.shape[1], Pi.ctypes.data,
+                            Pi.shape[0], 0)
+    return rc, h.value
+
+
+@pytest.mark.parametrize("N,k,d", [(12, 2, 64), (1, 2, 64), (256, 3, 64), (256, 2, 96), (131072, 2, 64),
+                                   (65536, 2, 64), (16, 64, 64), (256, 128, 128)])
+def test_codebook_load_rejects_unsupported_shapes(L, N, k, d):
+    rc, h = _load(L, np.zeros((N, k)), np.eye(d))
+    assert rc == fb.FQ_EINVAL and not h
+
+
+def test_codebook_load_rejects_non_finite(L):
+    C = np.zeros((16, 2))
+    C[3, 1] = np.nan
+    assert _load(L, C, np.eye(64))[0] == fb.FQ_EINVAL
+    P = np.eye(64)
+    P[0, 5] = np.inf
+    assert _load(L, np.zeros((16, 2)), P)[0] == fb.FQ_EINVAL
+
+
+def test_codebook_load_without_gpu_reports_no_device(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc, h = _load(L, np.zeros((16, 2)), np.eye(64))
+    assert rc == fb.FQ_ENODEV and not h

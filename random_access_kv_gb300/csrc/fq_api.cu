@@ -43,6 +43,10 @@ void free_ctx(fq_ctx *c) {
     cudaFree(c->Pi);
     cudaFree(c->Crot);
     cudaFree(c->flags);
+    cudaFree(c->pi_split);
+    cudaFree(c->grid2);
+    cudaFree(c->pit_split);
+    cudaFree(c->cb_split);
     free(c);
 }
 
@@ -104,6 +108,7 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     c->B = B;
     c->nb = d / k;
     c->R = c->nb * B;
+    c->num_sms = prop.multiProcessorCount;
 
     std::vector<float> C(C_host, C_host + (size_t)N * k);
     std::vector<float> P(Pi_host, Pi_host + (size_t)d * d);
@@ -135,6 +140,8 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
     if (e == cudaSuccess) e = is_full(c) ? fq::prepare_full(c) : fq::prepare_encode_blocks(c);
     if (e == cudaSuccess && !is_full(c)) e = fq::prepare_decode_blocks(c);
+    if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
+    if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
     if (e != cudaSuccess) {
         const int rc = (e == cudaErrorMemoryAllocation) ? FQ_ENOMEM : FQ_ECUDA;
         free_ctx(c);
@@ -161,7 +168,7 @@ int fq_shape(const fq_ctx *ctx, int *d, int *k, int *N) {
 
 static int encode_common(fq_ctx *ctx, const void *x, int64_t M, fq::RowMap map, int64_t rows_total,
                          float *nu, uint32_t *codes, void *stream) {
-    if (!ctx || M < 0) return FQ_EINVAL;
+    if (!ctx || M < 0 || M > INT32_MAX) return FQ_EINVAL;
     if (M == 0) return FQ_OK;
     if (!x || !nu || !codes) return FQ_EINVAL;
     if (!aligned(x, 16) || !aligned(nu, 4) || !aligned(codes, 4)) return FQ_EALIGN;
@@ -169,8 +176,13 @@ static int encode_common(fq_ctx *ctx, const void *x, int64_t M, fq::RowMap map, 
     DeviceGuard g(ctx->device);
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = is_full(ctx) ? fq::launch_encode_full(ctx, (const __half *)x, M, map, nu, codes, s)
-                                 : fq::launch_encode_blocks(ctx, (const __half *)x, M, map, nu, codes, s);
+    cudaError_t e;
+    if (is_full(ctx))
+        e = fq::launch_encode_full(ctx, (const __half *)x, M, map, nu, codes, s);
+    else if (ctx->pi_split)
+        e = fq::launch_encode_k2_tc(ctx, (const __half *)x, M, map, nu, codes, s);
+    else
+        e = fq::launch_encode_blocks(ctx, (const __half *)x, M, map, nu, codes, s);
     return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
 }
 
@@ -203,8 +215,13 @@ static int decode_common(fq_ctx *ctx, const float *nu, const uint32_t *codes, in
     DeviceGuard g(ctx->device);
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = is_full(ctx) ? fq::launch_decode_full(ctx, nu, codes, M, idx, n, out, out_f32, s)
-                                 : fq::launch_decode_blocks(ctx, nu, codes, M, idx, n, out, out_f32, s);
+    cudaError_t e;
+    if (is_full(ctx))
+        e = fq::launch_decode_full(ctx, nu, codes, M, idx, n, out, out_f32, s);
+    else if (ctx->pit_split)
+        e = fq::launch_decode_tc(ctx, nu, codes, M, idx, n, out, out_f32, s);
+    else
+        e = fq::launch_decode_blocks(ctx, nu, codes, M, idx, n, out, out_f32, s);
     return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
 }
 

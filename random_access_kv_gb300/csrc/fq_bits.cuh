@@ -52,10 +52,11 @@ struct BitReader {
     uint64_t acc;
     int n;
 
-    __device__ __forceinline__ BitReader(const uint32_t *codes, int64_t bitpos)
+    // With active = false nothing is read (and get() must not be called).
+    __device__ __forceinline__ BitReader(const uint32_t *codes, int64_t bitpos, bool active = true)
         : words(codes), w((bitpos >> 5) + 1) {
         int off = (int)(bitpos & 31);
-        acc = (uint64_t)(__ldg(codes + (bitpos >> 5)) >> off);
+        acc = active ? (uint64_t)(__ldg(codes + (bitpos >> 5)) >> off) : 0ull;
         n = 32 - off;
     }
     __device__ __forceinline__ uint32_t get(int B) {

@@ -1,0 +1,335 @@
+// Tensor-core block decoder for k <= 8 [FibQuant §2.3, decoder], full and random-access
+// (gather, [FibQuant §1]: any vector decodes on its own from its fixed address).
+//
+// Per CTA: NG row groups of 128 threads, one thread per output vector (= TMEM lane), looping
+// over 128-row output tiles:
+//   1. Each thread reads its source row (idx[j] for a gather), its nu and its record, unpacks the
+//      d/k indices and writes the concatenated codewords y_hat, split into fp16 halves of
+//      2^10 y_hat (hi, lo), as row t of two shared-memory A operands (128-byte swizzle).
+//   2. One thread issues Y_hat Pi on the tensor pipe as three fp16 MMAs into a TMEM fp32
+//      accumulator: hi*Pi_hi + hi*Pi_lo + lo*Pi_hi, with Pi^T carried as fp16 halves of 2^12 Pi^T
+//      (the dropped lo*lo term is below 2^-22 of the result).
+//   3. Each thread reads its row back, scales it by nu 2^-22 and stores it (fp16 rounded to
+//      nearest even, or fp32).
+// Gather indices outside [0, M) give zero rows and set FQ_FLAG_RANGE.
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
+#include "fq_bits.cuh"
+#include "fq_internal.h"
+#include "fq_sm100.cuh"
+
+namespace fq {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kTileRows = 128;
+constexpr float kPiScale = 4096.f;    // 2^12 on Pi^T
+constexpr float kYScale = 1024.f;     // 2^10 on the codewords
+constexpr float kOutScale = 1.0f / (4096.f * 1024.f);
+
+template <int D, int K, int NG, bool CB_SMEM>
+struct DLayout {
+    static constexpr int kPiPart = D * D * 2;
+    static constexpr int kATile = kTileRows * D * 2;                 // one fp16 A operand
+    static constexpr int oPi = 0;
+    static constexpr int oA = oPi + 2 * kPiPart;
+    static constexpr int oCb = oA + NG * 2 * kATile;
+    static constexpr int kCbMax = CB_SMEM ? 16384 : 0;
+    static constexpr int oBar = oCb + kCbMax;
+    static constexpr int kBars = 1 + NG;
+    static constexpr int oTmem = oBar + kBars * 8;
+    static constexpr int kBytes = oTmem + 16 + 1024;
+    static constexpr uint32_t kTmemCols = (NG * D <= 64) ? 64 : (NG * D <= 128) ? 128 : (NG * D <= 256) ? 256 : 512;
+};
+
+struct DecParams {
+    const float *nu;
+    const uint32_t *codes;
+    int64_t M;
+    const int64_t *idx;       // null: row j
+    int64_t n;
+    int B;
+    int N;
+    const uint8_t *pit_split; // [2][D*D] fp16 halves of 2^12 Pi^T, swizzled
+    const uint16_t *cb;       // [N][2K] fp16: K hi halves then K lo halves of 2^10 c_n
+    void *out;
+    uint32_t *flags;
+};
+
+// Codeword n's hi and lo halves, K of each.
+template <int K>
+struct CwHalves {
+    uint32_t hi[K > 1 ? K / 2 : 1], lo[K > 1 ? K / 2 : 1];
+};
+
+template <int K, bool CB_SMEM>
+__device__ __forceinline__ CwHalves<K> fetch_cw(const uint16_t *cb, uint32_t n) {
+    CwHalves<K> r;
+    const uint16_t *p = cb + (size_t)n * 2 * K;
+    if constexpr (K == 8) {
+        const uint4 h = CB_SMEM ? *reinterpret_cast<const uint4 *>(p) : __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint4 l = CB_SMEM ? *reinterpret_cast<const uint4 *>(p + 8) : __ldg(reinterpret_cast<const uint4 *>(p + 8));
+        r.hi[0] = h.x; r.hi[1] = h.y; r.hi[2] = h.z; r.hi[3] = h.w;
+        r.lo[0] = l.x; r.lo[1] = l.y; r.lo[2] = l.z; r.lo[3] = l.w;
+    } else if constexpr (K == 4) {
+        const uint4 v = CB_SMEM ? *reinterpret_cast<const uint4 *>(p) : __ldg(reinterpret_cast<const uint4 *>(p));
+        r.hi[0] = v.x; r.hi[1] = v.y; r.lo[0] = v.z; r.lo[1] = v.w;
+    } else if constexpr (K == 2) {
+        const uint2 v = CB_SMEM ? *reinterpret_cast<const uint2 *>(p) : __ldg(reinterpret_cast<const uint2 *>(p));
+        r.hi[0] = v.x; r.lo[0] = v.y;
+    } else {
+        const uint32_t v = CB_SMEM ? *reinterpret_cast<const uint32_t *>(p) : __ldg(reinterpret_cast<const uint32_t *>(p));
+        r.hi[0] = v & 0xFFFFu; r.lo[0] = v >> 16;
+    }
+    return r;
+}
+
+template <int D, typename OutT>
+__device__ __forceinline__ void store16(OutT *out, int64_t j, int c, const float (&v)[16], float s) {
+    if constexpr (sizeof(OutT) == 2) {
+        uint4 *dst = reinterpret_cast<uint4 *>(out + j * D + 16 * c);
+        uint4 w[2];
+        __half2 *h = reinterpret_cast<__half2 *>(w);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) h[q] = __floats2half2_rn(v[2 * q] * s, v[2 * q + 1] * s);
+        dst[0] = w[0];
+        dst[1] = w[1];
+    } else {
+        float4 *dst = reinterpret_cast<float4 *>(out + j * D + 16 * c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q] * s, v[4 * q + 1] * s, v[4 * q + 2] * s, v[4 * q + 3] * s);
+    }
+}
+
+template <int D, int K, int NG, bool CB_SMEM, typename OutT>
+__global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
+    using L = DLayout<D, K, NG, CB_SMEM>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
+    const uint16_t *cb = CB_SMEM ? reinterpret_cast<const uint16_t *>(sm + L::oCb) : p.cb;
+
+    const int tid = threadIdx.x;
+    const int g = tid / 128;
+    const int t = tid % 128;
+    const int wq = t / 32;
+    uint64_t *bar_tab = bars;
+    uint64_t *bar_mma = bars + 1 + g;
+    uint8_t *a_hi = sm + L::oA + g * 2 * L::kATile;
+    uint8_t *a_lo = a_hi + L::kATile;
+
+    if (tid == 0) {
+        for (int i = 0; i < L::kBars; ++i) mbar_init(bars + i, 1);
+        fence_barrier_init();
+    }
+    if (tid < 32) tmem_alloc(tmem_slot, L::kTmemCols);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (tid == 0) {
+        const uint32_t cb_bytes = CB_SMEM ? (uint32_t)(p.N * K * 4) : 0u;
+        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + cb_bytes);
+        bulk_g2s(sm + L::oPi, p.pit_split, 2u * L::kPiPart, bar_tab);
+        if (CB_SMEM) bulk_g2s(sm + L::oCb, p.cb, cb_bytes, bar_tab);
+    }
+    bool ok = named_sync_and(1 + g, 128, mbar_wait(bar_tab, 0));
+
+    constexpr int NB = D / K;
+    const int R = NB * p.B;
+    const uint32_t idesc = idesc_f16_f32(128, D);
+    const uint32_t tmem_acc = tmem_base + (uint32_t)(g * D);
+    const uint32_t pb_hi = smem_addr(sm + L::oPi), pb_lo = pb_hi + L::kPiPart;
+    const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
+    const int64_t gstride = (int64_t)gridDim.x * NG;
+    OutT *out = reinterpret_cast<OutT *>(p.out);
+
+    int64_t it = 0;
+    for (int64_t tile = (int64_t)blockIdx.x * NG + g; tile < ntiles && ok; tile += gstride, ++it) {
+        const int64_t j = tile * kTileRows + t;
+        const bool live = j < p.n;
+        int64_t row = live ? (p.idx ? __ldg(p.idx + j) : j) : 0;
+        const bool valid = live && row >= 0 && row < p.M;
+        if (live && !valid) atomicOr(p.flags, (uint32_t)FQ_FLAG_RANGE);
+        const float s = valid ? __ldg(p.nu + row) * kOutScale : 0.f;
+        BitReader rd(p.codes, valid ? row * (int64_t)R : 0, valid);
+        // Row t of the two A operands, one 16-byte chunk (8 columns) at a time.
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+            if (valid) {
+                if constexpr (K >= 2) {
+#pragma unroll
+                    for (int b = 0; b < 8 / K; ++b) {
+                        const CwHalves<K> v = fetch_cw<K, CB_SMEM>(cb, rd.get(p.B));
+#pragma unroll
+                        for (int q = 0; q < K / 2; ++q) {
+                            hw[b * (K / 2) + q] = v.hi[q];
+                            lw[b * (K / 2) + q] = v.lo[q];
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 8; ++b) {
+                        const CwHalves<1> v = fetch_cw<1, CB_SMEM>(cb, rd.get(p.B));
+                        hw[b / 2] |= v.hi[0] << (16 * (b & 1));
+                        lw[b / 2] |= v.lo[0] << (16 * (b & 1));
+                    }
+                }
+            }
+            const int kb = c / 8, cc = c % 8;
+            const uint32_t off = (uint32_t)(kb * 16384 + t * 128 + ((cc ^ (t & 7)) << 4));
+            *reinterpret_cast<uint4 *>(a_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(a_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        fence_proxy_async_smem();
+        named_sync(1 + g, 128);
+        if (t == 0) {
+            tc_fence_after();
+            const uint32_t ah = smem_addr(a_hi), al = smem_addr(a_lo);
+#pragma unroll
+            for (int pass = 0; pass < 3; ++pass) {
+                const uint32_t aa = pass == 2 ? al : ah;
+                const uint32_t bb = pass == 1 ? pb_lo : pb_hi;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t aoff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
+                    const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
+                    mma_f16(tmem_acc, sdesc_sw128(aa + aoff), sdesc_sw128(bb + boff), idesc, (pass | kk) ? 1u : 0u);
+                }
+            }
+            mma_commit(bar_mma);
+        }
+        ok = named_sync_and(1 + g, 128, mbar_wait(bar_mma, (uint32_t)(it & 1)));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+            float v[16];
+            tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), v);
+            tmem_wait_ld();
+            if (live) store16<D, OutT>(out, j, c, v, s);
+        }
+        tc_fence_before();
+        named_sync(1 + g, 128);
+    }
+    if (!ok && t == 0) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+    __syncthreads();
+    if (!ok) mbar_wait(bar_mma, 0, 1000000ull);
+    tc_fence_after();
+    if (tid < 32) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
+template <int D, int K>
+constexpr int groups() { return D == 64 ? 4 : 2; }
+
+template <int D, int K>
+constexpr bool cb_in_smem() { return K <= 4; }
+
+template <int D, int K, typename OutT>
+cudaError_t launch_dk(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
+    constexpr int NG = groups<D, K>();
+    constexpr bool CBS = cb_in_smem<D, K>();
+    using L = DLayout<D, K, NG, CBS>;
+    const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
+    int64_t grid = (ntiles + NG - 1) / NG;
+    if (grid > ctx->num_sms) grid = ctx->num_sms;
+    decode_tc<D, K, NG, CBS, OutT><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int K>
+cudaError_t prep_dk() {
+    constexpr int NG = groups<D, K>();
+    constexpr bool CBS = cb_in_smem<D, K>();
+    using L = DLayout<D, K, NG, CBS>;
+    static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+}
+
+}  // namespace
+
+bool decode_tc_supported(const fq_ctx *ctx) {
+    if (!(ctx->d == 64 || ctx->d == 128)) return false;
+    if (!(ctx->k == 1 || ctx->k == 2 || ctx->k == 4 || ctx->k == 8)) return false;
+    // Codebooks that live in shared memory must fit its 16 KB slot.
+    if (ctx->k <= 4 && (size_t)ctx->N * ctx->k * 4 > 16384) return false;
+    return true;
+}
+
+cudaError_t prepare_decode_tc(fq_ctx *ctx) {
+    const int d = ctx->d, k = ctx->k, N = ctx->N;
+    std::vector<float> P((size_t)d * d), PT((size_t)d * d), C((size_t)N * k);
+    cudaError_t e = cudaMemcpy(P.data(), ctx->Pi, P.size() * 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(C.data(), ctx->C, C.size() * 4, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return e;
+    for (int a = 0; a < d; ++a)
+        for (int b = 0; b < d; ++b) PT[(size_t)a * d + b] = P[(size_t)b * d + a];
+    std::vector<uint16_t> pts;
+    split_operand_sw128(PT.data(), d, kPiScale, pts);
+    std::vector<uint16_t> cb((size_t)N * 2 * k);
+    for (int n = 0; n < N; ++n)
+        for (int q = 0; q < k; ++q) {
+            const float v = C[(size_t)n * k + q] * kYScale;
+            const __half hi = __float2half_rn(v);
+            const __half lo = __float2half_rn(v - __half2float(hi));
+            memcpy(&cb[(size_t)n * 2 * k + q], &hi, 2);
+            memcpy(&cb[(size_t)n * 2 * k + k + q], &lo, 2);
+        }
+    e = cudaMalloc((void **)&ctx->pit_split, pts.size() * 2);
+    if (e == cudaSuccess) e = cudaMemcpy(ctx->pit_split, pts.data(), pts.size() * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->cb_split, cb.size() * 2);
+    if (e == cudaSuccess) e = cudaMemcpy(ctx->cb_split, cb.data(), cb.size() * 2, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return e;
+#define PREP(D, K) prep_dk<D, K>()
+    if (d == 64) {
+        if (k == 1) return PREP(64, 1);
+        if (k == 2) return PREP(64, 2);
+        if (k == 4) return PREP(64, 4);
+        return PREP(64, 8);
+    }
+    if (k == 1) return PREP(128, 1);
+    if (k == 2) return PREP(128, 2);
+    if (k == 4) return PREP(128, 4);
+    return PREP(128, 8);
+#undef PREP
+}
+
+cudaError_t launch_decode_tc(const fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
+                             const int64_t *idx, int64_t n, void *out, bool out_f32, cudaStream_t s) {
+    DecParams p;
+    p.nu = nu;
+    p.codes = codes;
+    p.M = M;
+    p.idx = idx;
+    p.n = n;
+    p.B = ctx->B;
+    p.N = ctx->N;
+    p.pit_split = ctx->pit_split;
+    p.cb = ctx->cb_split;
+    p.out = out;
+    p.flags = ctx->flags;
+#define CALL(D, K) (out_f32 ? launch_dk<D, K, float>(ctx, p, s) : launch_dk<D, K, __half>(ctx, p, s))
+    if (ctx->d == 64) {
+        if (ctx->k == 1) return CALL(64, 1);
+        if (ctx->k == 2) return CALL(64, 2);
+        if (ctx->k == 4) return CALL(64, 4);
+        return CALL(64, 8);
+    }
+    if (ctx->k == 1) return CALL(128, 1);
+    if (ctx->k == 2) return CALL(128, 2);
+    if (ctx->k == 4) return CALL(128, 4);
+    return CALL(128, 8);
+#undef CALL
+}
+
+}  // namespace fq

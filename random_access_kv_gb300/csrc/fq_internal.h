@@ -1,9 +1,12 @@
 // Internal declarations shared by the translation units of libfq.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <vector>
 
 #include "../../include/fq.h"
 
@@ -15,6 +18,14 @@ struct fq_ctx {
     float *Pi;                   // [d x d] rotation, row-major
     float *Crot;                 // k == d: [N x d] rotated codebook C Pi (row n = Pi^T c_n)
     uint32_t *flags;             // sticky FQ_FLAG_* word
+    int num_sms;
+    // k = 2 tensor-core encoder tables
+    uint8_t *pi_split;           // fp16 halves of 2^12 Pi, swizzled as the MMA's B operand
+    uint32_t *grid2;             // candidate grid and overflow slots
+    float g_scale, g_offs;       // grid cell of u: round(u * g_scale + g_offs)
+    // tensor-core decoder tables
+    uint8_t *pit_split;          // fp16 halves of 2^12 Pi^T, swizzled as the MMA's B operand
+    uint16_t *cb_split;          // [N][2k] fp16 halves of 2^10 c_n (k hi, then k lo)
 };
 
 namespace fq {
@@ -42,6 +53,19 @@ cudaError_t launch_encode_full(const fq_ctx *ctx, const __half *x, int64_t M, Ro
 cudaError_t launch_decode_full(const fq_ctx *ctx, const float *nu, const uint32_t *codes,
                                int64_t M, const int64_t *idx, int64_t n, void *out,
                                bool out_f32, cudaStream_t s);
+// Tensor map of a row-major fp16 [M x D] matrix in 128-row x 64-column boxes, 128-byte swizzle.
+bool encode_rows_tensor_map(CUtensorMap *tm, const void *x, int64_t M, int D);
+// fp16 hi/lo halves of scale * src (d x d, row n = MMA row n) in the K-major 128-byte swizzle layout.
+void split_operand_sw128(const float *src, int d, float scale, std::vector<uint16_t> &out);
+
+bool k2_tc_supported(const fq_ctx *ctx);
+cudaError_t prepare_k2_tc(fq_ctx *ctx);
+cudaError_t launch_encode_k2_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
+                                uint32_t *codes, cudaStream_t s);
+bool decode_tc_supported(const fq_ctx *ctx);
+cudaError_t prepare_decode_tc(fq_ctx *ctx);
+cudaError_t launch_decode_tc(const fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
+                             const int64_t *idx, int64_t n, void *out, bool out_f32, cudaStream_t s);
 // One-time kernel attribute set-up (dynamic shared memory limits); called by fq_codebook_load.
 cudaError_t prepare_encode_blocks(const fq_ctx *ctx);
 cudaError_t prepare_decode_blocks(const fq_ctx *ctx);

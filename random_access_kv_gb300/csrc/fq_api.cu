@@ -45,6 +45,7 @@ void free_ctx(fq_ctx *c) {
     cudaFree(c->flags);
     cudaFree(c->pi_split);
     cudaFree(c->grid2);
+    cudaFree(c->cwx2);
     cudaFree(c->pit_split);
     cudaFree(c->cb_split);
     free(c);

@@ -106,7 +106,56 @@ __device__ __forceinline__ void store16(OutT *out, int64_t j, int c, const float
     }
 }
 
-template <int D, int K, int NG, bool CB_SMEM, typename OutT>
+// The source row, its scale and its record, loaded ahead of use. With a compile-time B whose
+// records are whole words (BS != 0) the record is held in registers; otherwise it is read
+// field by field through the bit reader when the A operand is written.
+template <int W>
+struct RowData {
+    int64_t j;
+    int64_t row;
+    bool live, valid;
+    float s;
+    uint32_t w[W > 0 ? W : 1];
+};
+
+template <int D, int K, int BS>
+__device__ __forceinline__ RowData<(BS ? (D / K) * BS / 32 : 0)> load_row(const DecParams &p, int64_t tile, int t) {
+    constexpr int W = BS ? (D / K) * BS / 32 : 0;
+    RowData<W> r;
+    r.j = tile * kTileRows + t;
+    r.live = r.j < p.n;
+    r.row = r.live ? (p.idx ? __ldg(p.idx + r.j) : r.j) : 0;
+    r.valid = r.live && r.row >= 0 && r.row < p.M;
+    r.s = r.valid ? __ldg(p.nu + r.row) * kOutScale : 0.f;
+    if constexpr (W > 0) {
+        const uint32_t *src = p.codes + (r.valid ? r.row : 0) * W;
+        if constexpr (W % 4 == 0) {
+            if ((reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0) {
+#pragma unroll
+                for (int q = 0; q < W; q += 4) {
+                    const uint4 v = r.valid ? __ldg(reinterpret_cast<const uint4 *>(src + q)) : make_uint4(0, 0, 0, 0);
+                    r.w[q] = v.x; r.w[q + 1] = v.y; r.w[q + 2] = v.z; r.w[q + 3] = v.w;
+                }
+                return r;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < W; ++q) r.w[q] = r.valid ? __ldg(src + q) : 0u;
+    }
+    return r;
+}
+
+// Field b (BS bits) of a register-held record.
+template <int BS, int W>
+__device__ __forceinline__ uint32_t field(const uint32_t (&w)[W], int b) {
+    const int bit = b * BS, q = bit / 32, o = bit % 32;
+    uint32_t v;
+    if (o + BS <= 32 || q + 1 >= W) v = w[q] >> o;
+    else v = __funnelshift_r(w[q], w[q + 1], o);
+    return v & ((1u << BS) - 1u);
+}
+
+template <int D, int K, int NG, bool CB_SMEM, int BS, typename OutT>
 __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
     using L = DLayout<D, K, NG, CB_SMEM>;
     extern __shared__ uint8_t smem_raw[];
@@ -124,6 +173,13 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
     uint64_t *bar_mma = bars + 1 + g;
     uint8_t *a_hi = sm + L::oA + g * 2 * L::kATile;
     uint8_t *a_lo = a_hi + L::kATile;
+    const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
+    const int64_t gstride = (int64_t)gridDim.x * NG;
+    const int64_t first = (int64_t)blockIdx.x * NG + g;
+    constexpr int W = BS ? (D / K) * BS / 32 : 0;
+
+    // The first tile's row data is requested before the tables arrive.
+    RowData<W> cur = load_row<D, K, BS>(p, first, t);
 
     if (tid == 0) {
         for (int i = 0; i < L::kBars; ++i) mbar_init(bars + i, 1);
@@ -146,38 +202,33 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
     const uint32_t idesc = idesc_f16_f32(128, D);
     const uint32_t tmem_acc = tmem_base + (uint32_t)(g * D);
     const uint32_t pb_hi = smem_addr(sm + L::oPi), pb_lo = pb_hi + L::kPiPart;
-    const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
-    const int64_t gstride = (int64_t)gridDim.x * NG;
     OutT *out = reinterpret_cast<OutT *>(p.out);
 
     int64_t it = 0;
-    for (int64_t tile = (int64_t)blockIdx.x * NG + g; tile < ntiles && ok; tile += gstride, ++it) {
-        const int64_t j = tile * kTileRows + t;
-        const bool live = j < p.n;
-        int64_t row = live ? (p.idx ? __ldg(p.idx + j) : j) : 0;
-        const bool valid = live && row >= 0 && row < p.M;
-        if (live && !valid) atomicOr(p.flags, (uint32_t)FQ_FLAG_RANGE);
-        const float s = valid ? __ldg(p.nu + row) * kOutScale : 0.f;
-        BitReader rd(p.codes, valid ? row * (int64_t)R : 0, valid);
+    for (int64_t tile = first; tile < ntiles && ok; tile += gstride, ++it) {
+        // Requests for the next tile go out now and land while this one is processed.
+        const RowData<W> nxt = load_row<D, K, BS>(p, tile + gstride, t);
+        if (cur.live && !cur.valid) atomicOr(p.flags, (uint32_t)FQ_FLAG_RANGE);
+        BitReader rd(p.codes, (BS == 0 && cur.valid) ? cur.row * (int64_t)R : 0, BS == 0 && cur.valid);
         // Row t of the two A operands, one 16-byte chunk (8 columns) at a time.
 #pragma unroll
         for (int c = 0; c < D / 8; ++c) {
             uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-            if (valid) {
-                if constexpr (K >= 2) {
+            if (cur.valid) {
+                constexpr int BPC = K >= 2 ? 8 / K : 8;      // blocks per chunk
 #pragma unroll
-                    for (int b = 0; b < 8 / K; ++b) {
-                        const CwHalves<K> v = fetch_cw<K, CB_SMEM>(cb, rd.get(p.B));
+                for (int b = 0; b < BPC; ++b) {
+                    uint32_t i;
+                    if constexpr (BS != 0) i = field<BS, W>(cur.w, c * BPC + b);
+                    else i = rd.get(p.B);
+                    const CwHalves<K> v = fetch_cw<K, CB_SMEM>(cb, i);
+                    if constexpr (K >= 2) {
 #pragma unroll
                         for (int q = 0; q < K / 2; ++q) {
                             hw[b * (K / 2) + q] = v.hi[q];
                             lw[b * (K / 2) + q] = v.lo[q];
                         }
-                    }
-                } else {
-#pragma unroll
-                    for (int b = 0; b < 8; ++b) {
-                        const CwHalves<1> v = fetch_cw<1, CB_SMEM>(cb, rd.get(p.B));
+                    } else {
                         hw[b / 2] |= v.hi[0] << (16 * (b & 1));
                         lw[b / 2] |= v.lo[0] << (16 * (b & 1));
                     }
@@ -214,10 +265,11 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
             float v[16];
             tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), v);
             tmem_wait_ld();
-            if (live) store16<D, OutT>(out, j, c, v, s);
+            if (cur.live) store16<D, OutT>(out, cur.j, c, v, cur.s);
         }
         tc_fence_before();
         named_sync(1 + g, 128);
+        cur = nxt;
     }
     if (!ok && t == 0) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
     __syncthreads();
@@ -232,7 +284,7 @@ constexpr int groups() { return D == 64 ? 4 : 2; }
 template <int D, int K>
 constexpr bool cb_in_smem() { return K <= 4; }
 
-template <int D, int K, typename OutT>
+template <int D, int K, int BS, typename OutT>
 cudaError_t launch_dk(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
     constexpr int NG = groups<D, K>();
     constexpr bool CBS = cb_in_smem<D, K>();
@@ -240,20 +292,31 @@ cudaError_t launch_dk(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
     const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
     int64_t grid = (ntiles + NG - 1) / NG;
     if (grid > ctx->num_sms) grid = ctx->num_sms;
-    decode_tc<D, K, NG, CBS, OutT><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(p);
+    decode_tc<D, K, NG, CBS, BS, OutT><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, int K>
+template <int D, int K, int BS>
 cudaError_t prep_dk() {
     constexpr int NG = groups<D, K>();
     constexpr bool CBS = cb_in_smem<D, K>();
     using L = DLayout<D, K, NG, CBS>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, BS, __half>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, float>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    return cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, BS, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kBytes);
+}
+
+// Record widths with a compile-time field size: (d, k, B) of the synthetic workloads, whose
+// records are whole 32-bit words. Everything else reads its fields at run time.
+constexpr int kStatic[][3] = {{64, 2, 4}, {64, 2, 8}, {64, 4, 10}, {128, 8, 12}};
+
+int static_bits(int d, int k, int B) {
+    for (const auto &c : kStatic)
+        if (c[0] == d && c[1] == k && c[2] == B) return B;
+    return 0;
 }
 
 }  // namespace
@@ -290,7 +353,15 @@ cudaError_t prepare_decode_tc(fq_ctx *ctx) {
     if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->cb_split, cb.size() * 2);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->cb_split, cb.data(), cb.size() * 2, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return e;
-#define PREP(D, K) prep_dk<D, K>()
+    {
+        cudaError_t es = cudaSuccess;
+        if (static_bits(d, k, ctx->B) == 4) es = prep_dk<64, 2, 4>();
+        if (static_bits(d, k, ctx->B) == 8) es = prep_dk<64, 2, 8>();
+        if (static_bits(d, k, ctx->B) == 10) es = prep_dk<64, 4, 10>();
+        if (static_bits(d, k, ctx->B) == 12) es = prep_dk<128, 8, 12>();
+        if (es != cudaSuccess) return es;
+    }
+#define PREP(D, K) prep_dk<D, K, 0>()
     if (d == 64) {
         if (k == 1) return PREP(64, 1);
         if (k == 2) return PREP(64, 2);
@@ -318,7 +389,16 @@ cudaError_t launch_decode_tc(const fq_ctx *ctx, const float *nu, const uint32_t 
     p.cb = ctx->cb_split;
     p.out = out;
     p.flags = ctx->flags;
-#define CALL(D, K) (out_f32 ? launch_dk<D, K, float>(ctx, p, s) : launch_dk<D, K, __half>(ctx, p, s))
+#define CALLB(D, K, BS) (out_f32 ? launch_dk<D, K, BS, float>(ctx, p, s) : launch_dk<D, K, BS, __half>(ctx, p, s))
+    switch (static_bits(ctx->d, ctx->k, ctx->B)) {
+        case 4: return CALLB(64, 2, 4);
+        case 8: return CALLB(64, 2, 8);
+        case 10: return CALLB(64, 4, 10);
+        case 12: return CALLB(128, 8, 12);
+        default: break;
+    }
+#undef CALLB
+#define CALL(D, K) (out_f32 ? launch_dk<D, K, 0, float>(ctx, p, s) : launch_dk<D, K, 0, __half>(ctx, p, s))
     if (ctx->d == 64) {
         if (ctx->k == 1) return CALL(64, 1);
         if (ctx->k == 2) return CALL(64, 2);

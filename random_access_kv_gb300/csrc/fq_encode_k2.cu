@@ -11,10 +11,11 @@
 //   4. Every thread reads its row of Y from TMEM, forms u = Y / (2^12 nu) block by block and
 //      finds each block's nearest codeword exactly. A 128 x 128 grid over the block plane lists,
 //      per cell, every codeword that can be nearest to some point of the cell (built on the host
-//      from exact box-distance bounds). A cell with a single candidate answers without touching
-//      the codebook; otherwise its candidates (up to four in the cell word, up to twelve in an
-//      overflow slot) are compared by squared difference |u_b - c|^2, ties to the lowest index.
-//      Points outside the grid fall back to a scan of the whole codebook.
+//      from exact box-distance bounds), at most four per cell word. The common path is
+//      branch-free: cell lookup, then the listed candidates scored by |c|^2 - 2 u.c (the |u|^2
+//      term is shared), ties to the lowest index. Cells with more candidates, and a ring of cells
+//      around the grid that catches points outside it, are marked; marked blocks are redone
+//      afterwards by squared difference over an overflow list or the whole codebook.
 //   5. Indices are packed LSB-first at the record's fixed bit address; nu is stored.
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -32,11 +33,15 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kGrid = 128;                 // grid cells per axis
+constexpr int kGrid = 128;                 // grid cells per axis inside the ring
+constexpr int kGridR = kGrid + 2;          // with the ring of marker cells
 constexpr int kTileRows = 128;
 constexpr float kPiScale = 4096.f;         // 2^12: keeps the fp16 low half of Pi out of subnormals
 constexpr int kOvfSlots = 64;              // cells with 5..12 candidates
 constexpr int kOvfMax = 12;
+constexpr int kCellBytes = (kGridR * kGridR * 4 + 15) & ~15;
+constexpr float kMagic = 12582912.f;       // 1.5 * 2^23: adding it rounds to an integer held in the low bits
+constexpr int kMagicBits = 0x4B400000;
 
 template <int D, int NG, int NBUF>
 struct Layout {
@@ -45,10 +50,10 @@ struct Layout {
     static constexpr int oPi = 0;
     static constexpr int oX = oPi + 2 * kPiPart;
     static constexpr int oGrid = oX + NG * NBUF * kXTile;
-    static constexpr int oOvf = oGrid + kGrid * kGrid * 4;
+    static constexpr int oOvf = oGrid + kCellBytes;
     static constexpr int oCw = oOvf + kOvfSlots * 16;
-    static constexpr int kCwMax = 256 * 8;
-    static constexpr int oBar = oCw + kCwMax;
+    static constexpr int oCwx = oCw + 256 * 8;
+    static constexpr int oBar = oCwx + 256 * 16;
     static constexpr int kBars = 1 + NG * NBUF + NG;
     static constexpr int oTmem = oBar + kBars * 8;
     static constexpr int kBytes = oTmem + 16 + 1024;             // + alignment slack
@@ -61,15 +66,16 @@ struct K2Params {
     RowMap map;
     int N, B;
     const uint8_t *pi_split;   // [2][D*D] fp16, pre-swizzled
-    const uint32_t *tables;    // [kGrid*kGrid] cell words, then [kOvfSlots][4] overflow slots
-    const float2 *cw;          // [N] codewords
+    const uint32_t *tables;    // kCellBytes of cell words, then [kOvfSlots][4] overflow slots
+    const float2 *cw;          // [N] codewords (exact rescans)
+    const float4 *cwx;         // [N] (-2 c0, -2 c1, |c|^2, 0): candidate scores
     float gscale, goffs;
     float *nu;
     uint32_t *codes;
     uint32_t *flags;
 };
 
-__device__ __forceinline__ void score(float u0, float u1, float2 c, uint32_t n, float &best, uint32_t &bi) {
+__device__ __forceinline__ void diff_score(float u0, float u1, float2 c, uint32_t n, float &best, uint32_t &bi) {
     const float e0 = u0 - c.x, e1 = u1 - c.y;
     const float s = fmaf(e1, e1, e0 * e0);
     if (s < best) {
@@ -78,56 +84,64 @@ __device__ __forceinline__ void score(float u0, float u1, float2 c, uint32_t n, 
     }
 }
 
-__device__ __noinline__ uint32_t scan_all(float u0, float u1, const float2 *cw, int N) {
-    float best = INFINITY;
-    uint32_t bi = 0;
-    for (int n = 0; n < N; ++n) score(u0, u1, cw[n], (uint32_t)n, best, bi);
-    return bi;
-}
-
-// A cell with more than four candidates is marked by a first byte above its last byte (a real
-// entry ascends and is padded with its first byte); its second byte names an overflow slot
-// (0xFF: none, scan the whole codebook).
-__device__ __noinline__ uint32_t overflow_cell(float u0, float u1, uint32_t e, const uint4 *ovf, const float2 *cw,
-                                               int N) {
+// Slow path for a marked cell: its overflow slot, or (slot 0xFF: ring cell or no slot left)
+// the whole codebook, compared by squared difference.
+__device__ __noinline__ uint32_t marked_cell(float u0, float u1, uint32_t e, const uint4 *ovf, const float2 *cw,
+                                             int N) {
     const uint32_t slot = (e >> 8) & 0xFFu;
-    if (slot >= (uint32_t)kOvfSlots) return scan_all(u0, u1, cw, N);
-    const uint4 o = ovf[slot];
     float best = INFINITY;
     uint32_t bi = 0;
+    if (slot >= (uint32_t)kOvfSlots) {
+        for (int n = 0; n < N; ++n) diff_score(u0, u1, cw[n], (uint32_t)n, best, bi);
+        return bi;
+    }
+    const uint4 o = ovf[slot];
     for (uint32_t q = 0; q < o.x; ++q) {
         const uint32_t w = q < 4 ? o.y : (q < 8 ? o.z : o.w);
         const uint32_t n = (w >> (8 * (q & 3))) & 0xFFu;
-        score(u0, u1, cw[n], n, best, bi);
+        diff_score(u0, u1, cw[n], n, best, bi);
     }
     return bi;
 }
 
-__device__ __forceinline__ uint32_t nearest2(float u0, float u1, const uint32_t *grid, const uint4 *ovf,
-                                             const float2 *cw, int N, float gs, float go) {
-    const float gx = fmaf(u0, gs, go);
-    const float gy = fmaf(u1, gs, go);
-    const int ix = __float_as_int(gx + 12582912.f) - 0x4B400000;   // round to the nearest integer
-    const int iy = __float_as_int(gy + 12582912.f) - 0x4B400000;
-    if ((unsigned)ix >= (unsigned)kGrid || (unsigned)iy >= (unsigned)kGrid) return scan_all(u0, u1, cw, N);
-    const uint32_t e = grid[iy * kGrid + ix];
-    const uint32_t b0 = e & 0xFFu;
-    if (b0 > (e >> 24)) return overflow_cell(u0, u1, e, ovf, cw, N);
+// Candidate scoring of one block. Returns the index; sets `marked` for marker cells (first byte
+// above last byte: impossible for a real entry, whose bytes ascend and are padded with the first).
+__device__ __forceinline__ uint32_t fast_block(float a0, float a1, float s, float sg, float gom,
+                                               const uint32_t *grid, const float4 *cwx, uint32_t &e_out,
+                                               bool &marked) {
+    const float lo = kMagic, hi = kMagic + (float)(kGridR - 1);
+    const float gx = fminf(fmaxf(fmaf(a0, sg, gom), lo), hi);
+    const float gy = fminf(fmaxf(fmaf(a1, sg, gom), lo), hi);
+    const int cell = (__float_as_int(gy) - kMagicBits) * kGridR + (__float_as_int(gx) - kMagicBits);
+    const uint32_t e = grid[cell];
+    e_out = e;
+    const float u0 = a0 * s, u1 = a1 * s;
+    const uint32_t b0 = e & 0xFFu, b1 = (e >> 8) & 0xFFu, b2 = (e >> 16) & 0xFFu, b3 = e >> 24;
+    marked = b0 > b3;
     uint32_t bi = b0;
-    if (((e >> 8) & 0xFFu) != b0) {              // more than one candidate
-        const float2 c0 = cw[b0];
-        const float e0 = u0 - c0.x, e1 = u1 - c0.y;
-        float best = fmaf(e1, e1, e0 * e0);
-#pragma unroll
-        for (int q = 1; q < 4; ++q) {
-            const uint32_t n = (e >> (8 * q)) & 0xFFu;
-            if (n != b0) score(u0, u1, cw[n], n, best, bi);
+    if (b1 != b0) {
+        const float4 c0 = cwx[b0];
+        float best = fmaf(u1, c0.y, fmaf(u0, c0.x, c0.z));
+        const float4 c1 = cwx[b1];
+        const float s1 = fmaf(u1, c1.y, fmaf(u0, c1.x, c1.z));
+        if (s1 < best) { best = s1; bi = b1; }
+        if (b2 != b0) {
+            const float4 c2 = cwx[b2];
+            const float s2 = fmaf(u1, c2.y, fmaf(u0, c2.x, c2.z));
+            if (s2 < best) { best = s2; bi = b2; }
+        }
+        if (b3 != b0) {
+            const float4 c3 = cwx[b3];
+            const float s3 = fmaf(u1, c3.y, fmaf(u0, c3.x, c3.z));
+            if (s3 < best) { best = s3; bi = b3; }
         }
     }
     return bi;
 }
 
-template <int D, int NG, int NBUF>
+// BS = log2 N when it divides 32 (records then hold whole 32/BS-index words: packed in
+// registers and stored as words); BS = 0 packs a run-time B through the bit writer.
+template <int D, int NG, int NBUF, int BS>
 __global__ void __launch_bounds__(NG * 128, 1)
 encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     using L = Layout<D, NG, NBUF>;
@@ -138,6 +152,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     uint32_t *grid = reinterpret_cast<uint32_t *>(sm + L::oGrid);
     uint4 *ovf = reinterpret_cast<uint4 *>(sm + L::oOvf);
     float2 *cw = reinterpret_cast<float2 *>(sm + L::oCw);
+    float4 *cwx = reinterpret_cast<float4 *>(sm + L::oCwx);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
     uint64_t *bar_tab = bars;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
@@ -165,12 +180,13 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
 
     if (tid == 0) {
         prefetch_tensormap(&xmap);
-        const uint32_t cw_bytes = (uint32_t)((p.N * 8 + 15) & ~15);
-        const uint32_t tab_bytes = kGrid * kGrid * 4u + kOvfSlots * 16u;
-        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + tab_bytes + cw_bytes);
+        const uint32_t cw_bytes = (uint32_t)p.N * 8u, cwx_bytes = (uint32_t)p.N * 16u;
+        const uint32_t tab_bytes = kCellBytes + kOvfSlots * 16u;
+        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + tab_bytes + cw_bytes + cwx_bytes);
         bulk_g2s(pi, p.pi_split, 2u * L::kPiPart, bar_tab);
         bulk_g2s(grid, p.tables, tab_bytes, bar_tab);
         bulk_g2s(cw, p.cw, cw_bytes, bar_tab);
+        bulk_g2s(cwx, p.cwx, cwx_bytes, bar_tab);
     }
     // Each row group's first x tile.
     if (t == 0 && first < ntiles) {
@@ -185,6 +201,8 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     const uint32_t tmem_acc = tmem_base + (uint32_t)(g * D);
     const uint32_t pi_hi = smem_addr(pi), pi_lo = pi_hi + L::kPiPart;
     const int R = (D / 2) * p.B;
+    // +1: cell (i, j) sits at (i+1, j+1) inside the ring. goffs is an integer, so this is exact.
+    const float gom = p.goffs + 1.0f + kMagic;
 
     int64_t it = 0;
     for (int64_t tile = first; tile < ntiles && ok; tile += gstride, ++it) {
@@ -194,8 +212,8 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         if (!ok) break;
         const int64_t next = tile + gstride;
         if (NBUF == 2 && t == 0 && next < ntiles) {
-            // The other buffer's last reader (tile it-1: MMA and nu) finished before the group
-            // barrier that closed iteration it-1.
+            // The other buffer's last readers (tile it-1: its MMA and the nu loads) finished
+            // before the group barrier that closed iteration it-1.
             uint8_t *xn = xbuf0 + (buf ^ 1) * L::kXTile;
             mbar_arrive_expect_tx(bar_load + (buf ^ 1), (uint32_t)L::kXTile);
 #pragma unroll
@@ -244,23 +262,66 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         const bool finite = isfinite(ss);
         const float nu = finite ? sqrtf(ss) : 0.f;
         const float s = nu > 0.f ? (1.0f / kPiScale) / nu : 0.f;
+        const float sg = s * p.gscale;
+        const bool zero = !(nu > 0.f);
         const int64_t orow = live ? p.map(r) : 0;
+        constexpr int W = BS ? (D / 2) * BS / 32 : 1;   // record words (static packing)
+        uint32_t words[W];
+#pragma unroll
+        for (int w = 0; w < W; ++w) words[w] = 0u;
         BitWriter wr(p.codes, orow * (int64_t)R);
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < D / 16; ++c) {
             float a[16];
             tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), a);
             tmem_wait_ld();
-            if (live) {
+            uint32_t idx[8], ent[8];
+            uint32_t marks = 0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t i = nearest2(a[2 * j] * s, a[2 * j + 1] * s, grid, ovf, cw, p.N, p.gscale, p.goffs);
-                    wr.put(nu > 0.f ? i : 0u, p.B);
+            for (int j = 0; j < 8; ++j) {
+                bool m;
+                idx[j] = fast_block(a[2 * j], a[2 * j + 1], s, sg, gom, grid, cwx, ent[j], m);
+                marks |= (uint32_t)m << j;
+            }
+            if (marks && live && !zero) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if ((marks >> j) & 1u) idx[j] = marked_cell(a[2 * j] * s, a[2 * j + 1] * s, ent[j], ovf, cw, p.N);
+            }
+            if constexpr (BS != 0) {
+                // 8 indices of BS bits: bits [c * 8 BS, (c+1) * 8 BS) of the record.
+                uint64_t acc = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc |= (uint64_t)(zero ? 0u : idx[j]) << (j * BS);
+                constexpr int kBits = 8 * BS;
+                const int bit0 = c * kBits;
+                if constexpr (kBits >= 32) {
+#pragma unroll
+                    for (int q = 0; q < kBits / 32; ++q) words[bit0 / 32 + q] = (uint32_t)(acc >> (32 * q));
+                } else {
+                    words[bit0 / 32] |= (uint32_t)acc << (bit0 % 32);
+                }
+            } else {
+                if (live) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) wr.put(zero ? 0u : idx[j], p.B);
                 }
             }
         }
         if (live) {
-            wr.flush();
+            if constexpr (BS != 0) {
+                uint32_t *dst = p.codes + orow * (int64_t)W;
+                if ((W % 4) == 0 && ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0)) {
+#pragma unroll
+                    for (int w = 0; w < W; w += 4)
+                        *reinterpret_cast<uint4 *>(dst + w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < W; ++w) dst[w] = words[w];
+                }
+            } else {
+                wr.flush();
+            }
             p.nu[orow] = nu;
             if (!finite) atomicOr(p.flags, (uint32_t)FQ_FLAG_NONFINITE);
         }
@@ -284,7 +345,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     if (tid < 32) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
-template <int D, int NG, int NBUF>
+template <int D, int NG, int NBUF, int BS>
 cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu, uint32_t *codes,
                       cudaStream_t s) {
     using L = Layout<D, NG, NBUF>;
@@ -298,6 +359,7 @@ cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     p.pi_split = ctx->pi_split;
     p.tables = ctx->grid2;
     p.cw = reinterpret_cast<const float2 *>(ctx->C);
+    p.cwx = reinterpret_cast<const float4 *>(ctx->cwx2);
     p.gscale = ctx->g_scale;
     p.goffs = ctx->g_offs;
     p.nu = nu;
@@ -306,15 +368,40 @@ cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     const int64_t ntiles = (M + kTileRows - 1) / kTileRows;
     int64_t grid = (ntiles + NG - 1) / NG;
     if (grid > ctx->num_sms) grid = ctx->num_sms;
-    encode_k2_tc<D, NG, NBUF><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(tm, p);
+    encode_k2_tc<D, NG, NBUF, BS><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(tm, p);
     return cudaGetLastError();
 }
 
-template <int D, int NG, int NBUF>
+template <int D, int NG, int NBUF, int BS>
 cudaError_t prep_k2() {
     using L = Layout<D, NG, NBUF>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
-    return cudaFuncSetAttribute(encode_k2_tc<D, NG, NBUF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    return cudaFuncSetAttribute(encode_k2_tc<D, NG, NBUF, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kBytes);
+}
+
+// Static packing when B divides 32 (B = 1, 2, 4, 8); the generic bit writer otherwise.
+template <int D, int NG, int NBUF>
+cudaError_t dispatch_prep(int B) {
+    switch (B) {
+        case 1: return prep_k2<D, NG, NBUF, 1>();
+        case 2: return prep_k2<D, NG, NBUF, 2>();
+        case 4: return prep_k2<D, NG, NBUF, 4>();
+        case 8: return prep_k2<D, NG, NBUF, 8>();
+        default: return prep_k2<D, NG, NBUF, 0>();
+    }
+}
+
+template <int D, int NG, int NBUF>
+cudaError_t dispatch_launch(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu, uint32_t *codes,
+                            cudaStream_t s) {
+    switch (ctx->B) {
+        case 1: return launch_k2<D, NG, NBUF, 1>(ctx, x, M, map, nu, codes, s);
+        case 2: return launch_k2<D, NG, NBUF, 2>(ctx, x, M, map, nu, codes, s);
+        case 4: return launch_k2<D, NG, NBUF, 4>(ctx, x, M, map, nu, codes, s);
+        case 8: return launch_k2<D, NG, NBUF, 8>(ctx, x, M, map, nu, codes, s);
+        default: return launch_k2<D, NG, NBUF, 0>(ctx, x, M, map, nu, codes, s);
+    }
 }
 
 }  // namespace
@@ -322,8 +409,9 @@ cudaError_t prep_k2() {
 // Candidate grid for the k = 2 search. Cell (i, j) holds every codeword that is nearest to some
 // point of the cell's box (widened by a small margin against rounding of the cell index):
 // c_n qualifies iff its distance to the box is at most min_m (distance from c_m to the box's
-// farthest corner), a bound that holds for every point of the box. Layout: kGrid^2 cell words,
-// then kOvfSlots overflow slots of four words (count, then up to twelve index bytes).
+// farthest corner), a bound that holds for every point of the box. Layout: a (kGrid + 2)^2 array
+// of cell words whose outer ring marks points outside the grid, then kOvfSlots overflow slots of
+// four words (count, then up to twelve index bytes).
 static void build_k2_grid(const float *C, int N, int d, std::vector<uint32_t> &tab, float &gscale,
                           float &goffs) {
     // Grid half-width: the larger of the codebook's extent and the radius that a block of a
@@ -333,12 +421,18 @@ static void build_k2_grid(const float *C, int N, int d, std::vector<uint32_t> &t
     const double rq = sqrt(1.0 - pow(1e-7, 1.0 / (0.5 * d - 1.0)));
     const double Rg = fmax(1.05 * cmax, rq);
     const double eps = 1e-3 * (2.0 * Rg / kGrid);
-    gscale = (float)(kGrid / (2.0 * Rg));
-    goffs = (float)(0.5 * kGrid - 0.5);
-    // The device rounds u * gscale + goffs to the nearest integer; cell bounds follow from the
-    // fp32 constants it uses.
+    // The device rounds u * gscale + goffs to the nearest integer. goffs is an integer so that
+    // goffs + 1 + 1.5 * 2^23 (the device folds the ring offset and the rounding constant into one
+    // addend) stays exact in fp32; cell i then covers u * gscale + goffs in [i - 1/2, i + 1/2],
+    // and the 128 cells cover [-Rg, Rg]. Cell bounds follow from the fp32 constants.
+    goffs = (float)(kGrid / 2);
+    gscale = (float)((0.5 * kGrid - 0.5) / Rg);
     const double gs = gscale, go = goffs;
-    tab.assign((size_t)kGrid * kGrid + 4 * kOvfSlots, 0u);
+    const size_t cell_words = kCellBytes / 4;
+    const uint32_t ring = 0xFFu | (0xFFu << 8);          // marker, no slot: scan everything
+    tab.assign(cell_words + 4 * kOvfSlots, 0u);
+    for (int iy = 0; iy < kGridR; ++iy)
+        for (int ix = 0; ix < kGridR; ++ix) tab[(size_t)iy * kGridR + ix] = ring;
     std::vector<int> cand;
     int slots = 0;
     for (int iy = 0; iy < kGrid; ++iy) {
@@ -357,12 +451,12 @@ static void build_k2_grid(const float *C, int N, int d, std::vector<uint32_t> &t
                 const double dx = fmax(0.0, fmax(x0 - cx, cx - x1)), dy = fmax(0.0, fmax(y0 - cy, cy - y1));
                 if (dx * dx + dy * dy <= U2 * (1.0 + 1e-12)) cand.push_back(n);
             }
-            uint32_t &cell = tab[(size_t)iy * kGrid + ix];
+            uint32_t &cell = tab[(size_t)(iy + 1) * kGridR + (ix + 1)];
             if (cand.size() > 4) {
                 uint32_t slot = 0xFFu;
                 if (cand.size() <= (size_t)kOvfMax && slots < kOvfSlots) {
                     slot = (uint32_t)slots++;
-                    uint32_t *o = &tab[(size_t)kGrid * kGrid + 4 * slot];
+                    uint32_t *o = &tab[cell_words + 4 * slot];
                     o[0] = (uint32_t)cand.size();
                     for (size_t q = 0; q < cand.size(); ++q) o[1 + q / 4] |= (uint32_t)cand[q] << (8 * (q % 4));
                 }
@@ -376,7 +470,7 @@ static void build_k2_grid(const float *C, int N, int d, std::vector<uint32_t> &t
     }
 }
 
-// Pi (or Pi^T) as two fp16 halves of 2^12 Pi, each in the K-major 128-byte-swizzle layout the
+// Pi (or Pi^T) as two fp16 halves of scale * src, each in the K-major 128-byte-swizzle layout the
 // MMA reads as its B operand: B[n][k] = src[n][k]; element (n, k) lives in K-block k / 64,
 // row n (128 bytes), 16-byte chunk (k % 64) / 8 XOR (n % 8).
 void split_operand_sw128(const float *src, int d, float scale, std::vector<uint16_t> &out) {
@@ -435,19 +529,29 @@ cudaError_t prepare_k2_tc(fq_ctx *ctx) {
     if (e != cudaSuccess) return e;
     build_k2_grid(C.data(), ctx->N, ctx->d, tab, ctx->g_scale, ctx->g_offs);
     split_operand_sw128(P.data(), ctx->d, kPiScale, pis);
+    std::vector<float> cwx((size_t)ctx->N * 4);
+    for (int n = 0; n < ctx->N; ++n) {
+        const double c0 = C[2 * n], c1 = C[2 * n + 1];
+        cwx[4 * n + 0] = (float)(-2.0 * c0);
+        cwx[4 * n + 1] = (float)(-2.0 * c1);
+        cwx[4 * n + 2] = (float)(c0 * c0 + c1 * c1);
+        cwx[4 * n + 3] = 0.f;
+    }
     e = cudaMalloc((void **)&ctx->grid2, tab.size() * 4);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->grid2, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->pi_split, pis.size() * 2);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->pi_split, pis.data(), pis.size() * 2, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->cwx2, cwx.size() * 4);
+    if (e == cudaSuccess) e = cudaMemcpy(ctx->cwx2, cwx.data(), cwx.size() * 4, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return e;
-    if (ctx->d == 64) return prep_k2<64, 4, 2>();
-    return prep_k2<128, 2, 1>();
+    if (ctx->d == 64) return dispatch_prep<64, 4, 2>(ctx->B);
+    return dispatch_prep<128, 2, 1>(ctx->B);
 }
 
 cudaError_t launch_encode_k2_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                 uint32_t *codes, cudaStream_t s) {
-    if (ctx->d == 64) return launch_k2<64, 4, 2>(ctx, x, M, map, nu, codes, s);
-    return launch_k2<128, 2, 1>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64) return dispatch_launch<64, 4, 2>(ctx, x, M, map, nu, codes, s);
+    return dispatch_launch<128, 2, 1>(ctx, x, M, map, nu, codes, s);
 }
 
 }  // namespace fq

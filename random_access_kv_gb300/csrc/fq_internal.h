@@ -22,6 +22,7 @@ struct fq_ctx {
     // k = 2 tensor-core encoder tables
     uint8_t *pi_split;           // fp16 halves of 2^12 Pi, swizzled as the MMA's B operand
     uint32_t *grid2;             // candidate grid and overflow slots
+    float *cwx2;                 // [N x 4] (-2 c0, -2 c1, |c|^2, 0)
     float g_scale, g_offs;       // grid cell of u: round(u * g_scale + g_offs)
     // tensor-core decoder tables
     uint8_t *pit_split;          // fp16 halves of 2^12 Pi^T, swizzled as the MMA's B operand

@@ -1,7 +1,8 @@
 #!/usr/bin/env python3
 """Throughput of the FibQuant codec hot path on one GB300 (or N independent replicas).
 
-One step = the whole hot path over one batch of the GPT-2-small-shaped KV workload
+One step = the whole hot path over one batch of the GPT-2-small-shaped KV workload (the default;
+`--workload 1|3|5` times the other encode + full-decode workloads the same way)
 (12 layers x 12 heads x 1024 tokens, d = 64, k = 2, N = 256, b = 4 bits per coordinate):
 encode all of K and all of V (2 x 147,456 vectors: norm, rotation, nearest codeword, fixed-
 address packing), then random-access decode of 65,536 uniformly drawn rows from each
@@ -221,14 +222,19 @@ def run_ours(args) -> None:
 
     cfg = args.workload
     w = synth.WORKLOADS[cfg]
-    if w.op != "encode+gather":
-        raise SystemExit("bench times the encode + random-access decode workload (2)")
+    if w.op not in ("encode+gather", "encode+decode"):
+        raise SystemExit(f"workload {cfg} ({w.op}) is not timed by bench.py")
     C, Pi = pcb.for_workload(cfg)
     ctx = fq.fq_codebook_load(C, Pi, local)
     R = fq.fq_record_bits(ctx)
-    M, G, d = w.rows, w.gather, w.d
+    M, d = w.rows, w.d
+    # encode+decode workloads decode every row: a gather of all rows in order
+    G = w.gather if w.op == "encode+gather" else M
     x_host = [torch.from_numpy(synth.kv_tensor(cfg, t)).pin_memory() for t in range(w.tensors)]
-    i_host = [torch.from_numpy(synth.gather_indices(cfg, t, M, G)).pin_memory() for t in range(w.tensors)]
+    if w.op == "encode+gather":
+        i_host = [torch.from_numpy(synth.gather_indices(cfg, t, M, G)).pin_memory() for t in range(w.tensors)]
+    else:
+        i_host = [torch.arange(M, dtype=torch.int64).pin_memory() for _ in range(w.tensors)]
     xs = [h.to(dev) for h in x_host]
     idxs = [h.to(dev) for h in i_host]
     stores = [fq.alloc_store(ctx, M, dev) for _ in range(w.tensors)]
@@ -249,7 +255,10 @@ def run_ours(args) -> None:
             nu, codes = stores[t]
             if ev is not None:
                 ev[f"gat{t}"][0].record(stream)
-            fq.fq_decode_gather(ctx, nu, codes, M, idxs[t], G, outs[t], sp)
+            if w.op == "encode+gather":
+                fq.fq_decode_gather(ctx, nu, codes, M, idxs[t], G, outs[t], sp)
+            else:
+                fq.fq_decode(ctx, nu, codes, M, outs[t], sp)
             if ev is not None:
                 ev[f"gat{t}"][1].record(stream)
 
@@ -304,7 +313,8 @@ def run_ours(args) -> None:
     def e2e_step():
         for t in range(w.tensors):
             xs[t].copy_(x_host[t], non_blocking=True)
-            idxs[t].copy_(i_host[t], non_blocking=True)
+            if w.op == "encode+gather":
+                idxs[t].copy_(i_host[t], non_blocking=True)
         step()
         for t in range(w.tensors):
             nu_host[t].copy_(stores[t][0], non_blocking=True)
@@ -323,7 +333,7 @@ def run_ours(args) -> None:
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    h2d = sum(x.numel() * 2 + i.numel() * 8 for x, i in zip(x_host, i_host))
+    h2d = sum(x.numel() * 2 + (i.numel() * 8 if w.op == "encode+gather" else 0) for x, i in zip(x_host, i_host))
     d2h = sum(n.numel() * 4 + c.numel() * 4 + o.numel() * 2 for n, c, o in zip(nu_host, code_host, out_host))
     e2e_total = sum(e2e_ms)
     if world > 1:
@@ -333,21 +343,32 @@ def run_ours(args) -> None:
     e2e_value = world * vec_per_step * args.steps / (e2e_total / 1e3)
 
     enc_b, gat_b = workload_bytes(w, R)
+    if w.op != "encode+gather":
+        gat_b -= 8                          # a full decode reads no index array
     enc_ms = statistics.mean(kern["enc0"] + kern.get("enc1", []))
     gat_ms = statistics.mean(kern["gat0"] + kern.get("gat1", []))
     peaks = measured_peaks()
+    dec_name = "decode_gather" if w.op == "encode+gather" else "decode"
     if enc_ms * M >= gat_ms * G:
         dom, dom_bytes, dom_ms, kname = "encode", enc_b * M, enc_ms, "fq_encode"
     else:
-        dom, dom_bytes, dom_ms, kname = "decode_gather", gat_b * G, gat_ms, "fq_decode_gather"
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
+        dom, dom_bytes, dom_ms, kname = dec_name, gat_b * G, gat_ms, "fq_" + dec_name
+    roofline = {"kernel": dom, "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": int(dom_bytes), "launch_ms": round(dom_ms, 5),
-                "encode_launch_ms": round(enc_ms, 5), "gather_launch_ms": round(gat_ms, 5),
+                "encode_launch_ms": round(enc_ms, 5), f"{dec_name}_launch_ms": round(gat_ms, 5),
                 "encode_gbs": round(enc_b * M / (enc_ms / 1e3) / 1e9, 1),
-                "gather_gbs": round(gat_b * G / (gat_ms / 1e3) / 1e9, 1)}
+                f"{dec_name}_gbs": round(gat_b * G / (gat_ms / 1e3) / 1e9, 1)}
+    if dom == "encode" and w.k == w.d:
+        # The full-vector code's encode is a contraction with the rotated codebook: 2 M N d flops.
+        flops = 2.0 * M * w.N * d
+        achieved = flops / (dom_ms / 1e3) / 1e12
+        roofline.update({"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                         "algorithmic_flops_per_launch": flops})
+    else:
+        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        roofline.update({"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -361,7 +382,8 @@ def run_ours(args) -> None:
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "rows_per_tensor": M, "tensors": w.tensors, "d": d, "k": w.k,
-                       "N": w.N, "bits_per_coordinate": w.B / w.k, "record_bits": R, "gather_per_tensor": G,
+                       "N": w.N, "bits_per_coordinate": w.B / w.k, "record_bits": R,
+                       ("gather_per_tensor" if w.op == "encode+gather" else "decoded_per_tensor"): G,
                        "l2": "flushed before every timed step (256 MB write, outside the step events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "fp16_gbps": value * 2 * d / 1e9,

@@ -45,9 +45,9 @@ void free_ctx(fq_ctx *c) {
     cudaFree(c->flags);
     cudaFree(c->pi_split);
     cudaFree(c->grid2);
-    cudaFree(c->cwx2);
     cudaFree(c->pit_split);
     cudaFree(c->cb_split);
+    cudaFree(c->crot_split);
     free(c);
 }
 
@@ -143,6 +143,7 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     if (e == cudaSuccess && !is_full(c)) e = fq::prepare_decode_blocks(c);
     if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
     if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
+    if (e == cudaSuccess && is_full(c) && fq::full_tc_supported(c)) e = fq::prepare_full_tc(c);
     if (e != cudaSuccess) {
         const int rc = (e == cudaErrorMemoryAllocation) ? FQ_ENOMEM : FQ_ECUDA;
         free_ctx(c);
@@ -178,7 +179,9 @@ static int encode_common(fq_ctx *ctx, const void *x, int64_t M, fq::RowMap map, 
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e;
-    if (is_full(ctx))
+    if (is_full(ctx) && ctx->crot_split)
+        e = fq::launch_encode_full_tc(ctx, (const __half *)x, M, map, nu, codes, s);
+    else if (is_full(ctx))
         e = fq::launch_encode_full(ctx, (const __half *)x, M, map, nu, codes, s);
     else if (ctx->pi_split)
         e = fq::launch_encode_k2_tc(ctx, (const __half *)x, M, map, nu, codes, s);

@@ -12,8 +12,8 @@
 //      finds each block's nearest codeword exactly. A 128 x 128 grid over the block plane lists,
 //      per cell, every codeword that can be nearest to some point of the cell (built on the host
 //      from exact box-distance bounds), at most four per cell word. The common path is
-//      branch-free: cell lookup, then the listed candidates scored by |c|^2 - 2 u.c (the |u|^2
-//      term is shared), ties to the lowest index. Cells with more candidates, and a ring of cells
+//      branch-free: cell lookup, then the listed candidates compared by squared difference
+//      |u_b - c|^2, ties to the lowest index. Cells with more candidates, and a ring of cells
 //      around the grid that catches points outside it, are marked; marked blocks are redone
 //      afterwards by squared difference over an overflow list or the whole codebook.
 //   5. Indices are packed LSB-first at the record's fixed bit address; nu is stored.
@@ -52,8 +52,7 @@ struct Layout {
     static constexpr int oGrid = oX + NG * NBUF * kXTile;
     static constexpr int oOvf = oGrid + kCellBytes;
     static constexpr int oCw = oOvf + kOvfSlots * 16;
-    static constexpr int oCwx = oCw + 256 * 8;
-    static constexpr int oBar = oCwx + 256 * 16;
+    static constexpr int oBar = oCw + 256 * 8;
     static constexpr int kBars = 1 + NG * NBUF + NG;
     static constexpr int oTmem = oBar + kBars * 8;
     static constexpr int kBytes = oTmem + 16 + 1024;             // + alignment slack
@@ -67,8 +66,7 @@ struct K2Params {
     int N, B;
     const uint8_t *pi_split;   // [2][D*D] fp16, pre-swizzled
     const uint32_t *tables;    // kCellBytes of cell words, then [kOvfSlots][4] overflow slots
-    const float2 *cw;          // [N] codewords (exact rescans)
-    const float4 *cwx;         // [N] (-2 c0, -2 c1, |c|^2, 0): candidate scores
+    const float2 *cw;          // [N] codewords
     float gscale, goffs;
     float *nu;
     uint32_t *codes;
@@ -104,10 +102,12 @@ __device__ __noinline__ uint32_t marked_cell(float u0, float u1, uint32_t e, con
     return bi;
 }
 
-// Candidate scoring of one block. Returns the index; sets `marked` for marker cells (first byte
-// above last byte: impossible for a real entry, whose bytes ascend and are padded with the first).
+// Candidate scoring of one block by squared difference. Returns the index; sets `marked` for
+// marker cells (first byte above last byte: impossible for a real entry, whose bytes ascend and
+// are padded with the first). Candidates are 8-byte codeword loads, issued only for distinct
+// entries, so a single-candidate cell reads no codeword at all.
 __device__ __forceinline__ uint32_t fast_block(float a0, float a1, float s, float sg, float gom,
-                                               const uint32_t *grid, const float4 *cwx, uint32_t &e_out,
+                                               const uint32_t *grid, const float2 *cw, uint32_t &e_out,
                                                bool &marked) {
     const float lo = kMagic, hi = kMagic + (float)(kGridR - 1);
     const float gx = fminf(fmaxf(fmaf(a0, sg, gom), lo), hi);
@@ -120,21 +120,12 @@ __device__ __forceinline__ uint32_t fast_block(float a0, float a1, float s, floa
     marked = b0 > b3;
     uint32_t bi = b0;
     if (b1 != b0) {
-        const float4 c0 = cwx[b0];
-        float best = fmaf(u1, c0.y, fmaf(u0, c0.x, c0.z));
-        const float4 c1 = cwx[b1];
-        const float s1 = fmaf(u1, c1.y, fmaf(u0, c1.x, c1.z));
-        if (s1 < best) { best = s1; bi = b1; }
-        if (b2 != b0) {
-            const float4 c2 = cwx[b2];
-            const float s2 = fmaf(u1, c2.y, fmaf(u0, c2.x, c2.z));
-            if (s2 < best) { best = s2; bi = b2; }
-        }
-        if (b3 != b0) {
-            const float4 c3 = cwx[b3];
-            const float s3 = fmaf(u1, c3.y, fmaf(u0, c3.x, c3.z));
-            if (s3 < best) { best = s3; bi = b3; }
-        }
+        const float2 c0 = cw[b0];
+        const float d00 = u0 - c0.x, d01 = u1 - c0.y;
+        float best = fmaf(d01, d01, d00 * d00);
+        diff_score(u0, u1, cw[b1], b1, best, bi);
+        if (b2 != b0) diff_score(u0, u1, cw[b2], b2, best, bi);
+        if (b3 != b0) diff_score(u0, u1, cw[b3], b3, best, bi);
     }
     return bi;
 }
@@ -152,7 +143,6 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     uint32_t *grid = reinterpret_cast<uint32_t *>(sm + L::oGrid);
     uint4 *ovf = reinterpret_cast<uint4 *>(sm + L::oOvf);
     float2 *cw = reinterpret_cast<float2 *>(sm + L::oCw);
-    float4 *cwx = reinterpret_cast<float4 *>(sm + L::oCwx);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
     uint64_t *bar_tab = bars;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
@@ -180,13 +170,12 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
 
     if (tid == 0) {
         prefetch_tensormap(&xmap);
-        const uint32_t cw_bytes = (uint32_t)p.N * 8u, cwx_bytes = (uint32_t)p.N * 16u;
+        const uint32_t cw_bytes = (uint32_t)p.N * 8u;
         const uint32_t tab_bytes = kCellBytes + kOvfSlots * 16u;
-        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + tab_bytes + cw_bytes + cwx_bytes);
+        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + tab_bytes + cw_bytes);
         bulk_g2s(pi, p.pi_split, 2u * L::kPiPart, bar_tab);
         bulk_g2s(grid, p.tables, tab_bytes, bar_tab);
         bulk_g2s(cw, p.cw, cw_bytes, bar_tab);
-        bulk_g2s(cwx, p.cwx, cwx_bytes, bar_tab);
     }
     // Each row group's first x tile.
     if (t == 0 && first < ntiles) {
@@ -280,7 +269,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 bool m;
-                idx[j] = fast_block(a[2 * j], a[2 * j + 1], s, sg, gom, grid, cwx, ent[j], m);
+                idx[j] = fast_block(a[2 * j], a[2 * j + 1], s, sg, gom, grid, cw, ent[j], m);
                 marks |= (uint32_t)m << j;
             }
             if (marks && live && !zero) {
@@ -359,7 +348,6 @@ cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     p.pi_split = ctx->pi_split;
     p.tables = ctx->grid2;
     p.cw = reinterpret_cast<const float2 *>(ctx->C);
-    p.cwx = reinterpret_cast<const float4 *>(ctx->cwx2);
     p.gscale = ctx->g_scale;
     p.goffs = ctx->g_offs;
     p.nu = nu;
@@ -529,20 +517,10 @@ cudaError_t prepare_k2_tc(fq_ctx *ctx) {
     if (e != cudaSuccess) return e;
     build_k2_grid(C.data(), ctx->N, ctx->d, tab, ctx->g_scale, ctx->g_offs);
     split_operand_sw128(P.data(), ctx->d, kPiScale, pis);
-    std::vector<float> cwx((size_t)ctx->N * 4);
-    for (int n = 0; n < ctx->N; ++n) {
-        const double c0 = C[2 * n], c1 = C[2 * n + 1];
-        cwx[4 * n + 0] = (float)(-2.0 * c0);
-        cwx[4 * n + 1] = (float)(-2.0 * c1);
-        cwx[4 * n + 2] = (float)(c0 * c0 + c1 * c1);
-        cwx[4 * n + 3] = 0.f;
-    }
     e = cudaMalloc((void **)&ctx->grid2, tab.size() * 4);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->grid2, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->pi_split, pis.size() * 2);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->pi_split, pis.data(), pis.size() * 2, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->cwx2, cwx.size() * 4);
-    if (e == cudaSuccess) e = cudaMemcpy(ctx->cwx2, cwx.data(), cwx.size() * 4, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return e;
     if (ctx->d == 64) return dispatch_prep<64, 4, 2>(ctx->B);
     return dispatch_prep<128, 2, 1>(ctx->B);

@@ -22,11 +22,12 @@ struct fq_ctx {
     // k = 2 tensor-core encoder tables
     uint8_t *pi_split;           // fp16 halves of 2^12 Pi, swizzled as the MMA's B operand
     uint32_t *grid2;             // candidate grid and overflow slots
-    float *cwx2;                 // [N x 4] (-2 c0, -2 c1, |c|^2, 0)
     float g_scale, g_offs;       // grid cell of u: round(u * g_scale + g_offs)
     // tensor-core decoder tables
     uint8_t *pit_split;          // fp16 halves of 2^12 Pi^T, swizzled as the MMA's B operand
     uint16_t *cb_split;          // [N][2k] fp16 halves of 2^10 c_n (k hi, then k lo)
+    // k = d tensor-core encoder table
+    uint16_t *crot_split;        // [2][N x d] fp16 halves of -2 * 2^12 Crot (hi block, then lo block)
 };
 
 namespace fq {
@@ -67,6 +68,10 @@ bool decode_tc_supported(const fq_ctx *ctx);
 cudaError_t prepare_decode_tc(fq_ctx *ctx);
 cudaError_t launch_decode_tc(const fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
                              const int64_t *idx, int64_t n, void *out, bool out_f32, cudaStream_t s);
+bool full_tc_supported(const fq_ctx *ctx);
+cudaError_t prepare_full_tc(fq_ctx *ctx);
+cudaError_t launch_encode_full_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
+                                  uint32_t *codes, cudaStream_t s);
 // One-time kernel attribute set-up (dynamic shared memory limits); called by fq_codebook_load.
 cudaError_t prepare_encode_blocks(const fq_ctx *ctx);
 cudaError_t prepare_decode_blocks(const fq_ctx *ctx);

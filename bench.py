@@ -222,19 +222,35 @@ def run_ours(args) -> None:
 
     cfg = args.workload
     w = synth.WORKLOADS[cfg]
-    if w.op not in ("encode+gather", "encode+decode"):
+    if w.op not in ("encode+gather", "encode+decode", "stream+gather"):
         raise SystemExit(f"workload {cfg} ({w.op}) is not timed by bench.py")
+    stream = w.op == "stream+gather"
     C, Pi = pcb.for_workload(cfg)
     ctx = fq.fq_codebook_load(C, Pi, local)
     R = fq.fq_record_bits(ctx)
     M, d = w.rows, w.d
     # encode+decode workloads decode every row: a gather of all rows in order
-    G = w.gather if w.op == "encode+gather" else M
-    x_host = [torch.from_numpy(synth.kv_tensor(cfg, t)).pin_memory() for t in range(w.tensors)]
-    if w.op == "encode+gather":
-        i_host = [torch.from_numpy(synth.gather_indices(cfg, t, M, G)).pin_memory() for t in range(w.tensors)]
+    gathers = w.op != "encode+decode"
+    if stream:
+        # (layer, head) sequences of capacity T; each step appends `new` tokens to every sequence.
+        n_seq, T, new = w.rows // w.shape[-2], w.shape[-2], w.stream_new
+        n_steps = T // new
+        pos = synth.token_positions(cfg, T, w.gather)
+        gidx = torch.from_numpy((np.arange(n_seq)[:, None] * T + pos[None, :]).reshape(-1).astype(np.int64))
+        G = int(gidx.numel())
+
+        def arrival_order(a):  # [n_seq*T, d] -> [steps, n_seq*new, d], the order tokens arrive in
+            return np.ascontiguousarray(a.reshape(n_seq, n_steps, new, d).transpose(1, 0, 2, 3)).reshape(
+                n_steps, n_seq * new, d)
+        x_host = [torch.from_numpy(arrival_order(synth.kv_tensor(cfg, t))).pin_memory() for t in range(w.tensors)]
+        i_host = [gidx.pin_memory() for _ in range(w.tensors)]
     else:
-        i_host = [torch.arange(M, dtype=torch.int64).pin_memory() for _ in range(w.tensors)]
+        G = w.gather if gathers else M
+        x_host = [torch.from_numpy(synth.kv_tensor(cfg, t)).pin_memory() for t in range(w.tensors)]
+        if gathers:
+            i_host = [torch.from_numpy(synth.gather_indices(cfg, t, M, G)).pin_memory() for t in range(w.tensors)]
+        else:
+            i_host = [torch.arange(M, dtype=torch.int64).pin_memory() for _ in range(w.tensors)]
     xs = [h.to(dev) for h in x_host]
     idxs = [h.to(dev) for h in i_host]
     stores = [fq.alloc_store(ctx, M, dev) for _ in range(w.tensors)]
@@ -248,21 +264,26 @@ def run_ours(args) -> None:
             nu, codes = stores[t]
             if ev is not None:
                 ev[f"enc{t}"][0].record(stream)
-            fq.fq_encode(ctx, xs[t], M, nu, codes, 0, sp)
+            if stream:
+                for st in range(n_steps):
+                    fq.fq_encode_append(ctx, xs[t][st], n_seq, new, T, st * new, nu, codes, sp)
+            else:
+                fq.fq_encode(ctx, xs[t], M, nu, codes, 0, sp)
             if ev is not None:
                 ev[f"enc{t}"][1].record(stream)
         for t in range(w.tensors):
             nu, codes = stores[t]
             if ev is not None:
                 ev[f"gat{t}"][0].record(stream)
-            if w.op == "encode+gather":
+            if gathers:
                 fq.fq_decode_gather(ctx, nu, codes, M, idxs[t], G, outs[t], sp)
             else:
                 fq.fq_decode(ctx, nu, codes, M, outs[t], sp)
             if ev is not None:
                 ev[f"gat{t}"][1].record(stream)
 
-    launches_per_step = 2 * w.tensors
+    enc_launches = n_steps if stream else 1
+    launches_per_step = w.tensors * (enc_launches + 1)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
@@ -313,7 +334,7 @@ def run_ours(args) -> None:
     def e2e_step():
         for t in range(w.tensors):
             xs[t].copy_(x_host[t], non_blocking=True)
-            if w.op == "encode+gather":
+            if gathers:
                 idxs[t].copy_(i_host[t], non_blocking=True)
         step()
         for t in range(w.tensors):
@@ -333,7 +354,7 @@ def run_ours(args) -> None:
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    h2d = sum(x.numel() * 2 + (i.numel() * 8 if w.op == "encode+gather" else 0) for x, i in zip(x_host, i_host))
+    h2d = sum(x.numel() * 2 + (i.numel() * 8 if gathers else 0) for x, i in zip(x_host, i_host))
     d2h = sum(n.numel() * 4 + c.numel() * 4 + o.numel() * 2 for n, c, o in zip(nu_host, code_host, out_host))
     e2e_total = sum(e2e_ms)
     if world > 1:
@@ -343,24 +364,27 @@ def run_ours(args) -> None:
     e2e_value = world * vec_per_step * args.steps / (e2e_total / 1e3)
 
     enc_b, gat_b = workload_bytes(w, R)
-    if w.op != "encode+gather":
+    if not gathers:
         gat_b -= 8                          # a full decode reads no index array
-    enc_ms = statistics.mean(kern["enc0"] + kern.get("enc1", []))
+    # per launch: a streamed encode is n_steps append launches of M / n_steps rows each
+    enc_ms = statistics.mean(kern["enc0"] + kern.get("enc1", [])) / enc_launches
+    enc_rows = M // enc_launches
     gat_ms = statistics.mean(kern["gat0"] + kern.get("gat1", []))
     peaks = measured_peaks()
-    dec_name = "decode_gather" if w.op == "encode+gather" else "decode"
-    if enc_ms * M >= gat_ms * G:
-        dom, dom_bytes, dom_ms, kname = "encode", enc_b * M, enc_ms, "fq_encode"
+    dec_name = "decode_gather" if gathers else "decode"
+    if enc_ms * enc_launches * M >= gat_ms * G * enc_launches:
+        dom, dom_bytes, dom_ms = "encode", enc_b * enc_rows, enc_ms
+        kname = "fq_encode_append" if stream else "fq_encode"
     else:
         dom, dom_bytes, dom_ms, kname = dec_name, gat_b * G, gat_ms, "fq_" + dec_name
     roofline = {"kernel": dom, "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": int(dom_bytes), "launch_ms": round(dom_ms, 5),
                 "encode_launch_ms": round(enc_ms, 5), f"{dec_name}_launch_ms": round(gat_ms, 5),
-                "encode_gbs": round(enc_b * M / (enc_ms / 1e3) / 1e9, 1),
+                "encode_gbs": round(enc_b * enc_rows / (enc_ms / 1e3) / 1e9, 1),
                 f"{dec_name}_gbs": round(gat_b * G / (gat_ms / 1e3) / 1e9, 1)}
     if dom == "encode" and w.k == w.d:
         # The full-vector code's encode is a contraction with the rotated codebook: 2 M N d flops.
-        flops = 2.0 * M * w.N * d
+        flops = 2.0 * enc_rows * w.N * d
         achieved = flops / (dom_ms / 1e3) / 1e12
         roofline.update({"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
@@ -383,7 +407,9 @@ def run_ours(args) -> None:
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "rows_per_tensor": M, "tensors": w.tensors, "d": d, "k": w.k,
                        "N": w.N, "bits_per_coordinate": w.B / w.k, "record_bits": R,
-                       ("gather_per_tensor" if w.op == "encode+gather" else "decoded_per_tensor"): G,
+                       ("gather_per_tensor" if gathers else "decoded_per_tensor"): G,
+                       **({"append_steps": n_steps, "tokens_per_append": new, "sequences": n_seq}
+                          if stream else {}),
                        "l2": "flushed before every timed step (256 MB write, outside the step events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "fp16_gbps": value * 2 * d / 1e9,

@@ -224,14 +224,14 @@ def run_ours(args) -> None:
     w = synth.WORKLOADS[cfg]
     if w.op not in ("encode+gather", "encode+decode", "stream+gather"):
         raise SystemExit(f"workload {cfg} ({w.op}) is not timed by bench.py")
-    stream = w.op == "stream+gather"
+    streaming = w.op == "stream+gather"
     C, Pi = pcb.for_workload(cfg)
     ctx = fq.fq_codebook_load(C, Pi, local)
     R = fq.fq_record_bits(ctx)
     M, d = w.rows, w.d
     # encode+decode workloads decode every row: a gather of all rows in order
     gathers = w.op != "encode+decode"
-    if stream:
+    if streaming:
         # (layer, head) sequences of capacity T; each step appends `new` tokens to every sequence.
         n_seq, T, new = w.rows // w.shape[-2], w.shape[-2], w.stream_new
         n_steps = T // new
@@ -264,7 +264,7 @@ def run_ours(args) -> None:
             nu, codes = stores[t]
             if ev is not None:
                 ev[f"enc{t}"][0].record(stream)
-            if stream:
+            if streaming:
                 for st in range(n_steps):
                     fq.fq_encode_append(ctx, xs[t][st], n_seq, new, T, st * new, nu, codes, sp)
             else:
@@ -282,7 +282,7 @@ def run_ours(args) -> None:
             if ev is not None:
                 ev[f"gat{t}"][1].record(stream)
 
-    enc_launches = n_steps if stream else 1
+    enc_launches = n_steps if streaming else 1
     launches_per_step = w.tensors * (enc_launches + 1)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -374,7 +374,7 @@ def run_ours(args) -> None:
     dec_name = "decode_gather" if gathers else "decode"
     if enc_ms * enc_launches * M >= gat_ms * G * enc_launches:
         dom, dom_bytes, dom_ms = "encode", enc_b * enc_rows, enc_ms
-        kname = "fq_encode_append" if stream else "fq_encode"
+        kname = "fq_encode_append" if streaming else "fq_encode"
     else:
         dom, dom_bytes, dom_ms, kname = dec_name, gat_b * G, gat_ms, "fq_" + dec_name
     roofline = {"kernel": dom, "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
@@ -409,7 +409,7 @@ def run_ours(args) -> None:
                        "N": w.N, "bits_per_coordinate": w.B / w.k, "record_bits": R,
                        ("gather_per_tensor" if gathers else "decoded_per_tensor"): G,
                        **({"append_steps": n_steps, "tokens_per_append": new, "sequences": n_seq}
-                          if stream else {}),
+                          if streaming else {}),
                        "l2": "flushed before every timed step (256 MB write, outside the step events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "fp16_gbps": value * 2 * d / 1e9,

@@ -2,11 +2,12 @@
 """Throughput of the FibQuant codec hot path on one GB300 (or N independent replicas).
 
 One step = the whole hot path over one batch of the GPT-2-small-shaped KV workload (the default;
-`--workload 1|3|5` times the other encode + full-decode workloads the same way)
+`--workload 1|3|4|5` times the other workloads the same way)
 (12 layers x 12 heads x 1024 tokens, d = 64, k = 2, N = 256, b = 4 bits per coordinate):
 encode all of K and all of V (2 x 147,456 vectors: norm, rotation, nearest codeword, fixed-
 address packing), then random-access decode of 65,536 uniformly drawn rows from each
-(gather, unpack, codeword lookup, inverse rotation, scaling). Inputs are resident in HBM when
+(gather, unpack, codeword lookup, inverse rotation, scaling). K and V share the codebook and
+live in one code store, so each step is one encode launch and one gather launch. Inputs are resident in HBM when
 the timed region starts; L2 is flushed (a 256 MB write) before every timed step, outside the
 step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it.
 
@@ -225,65 +226,62 @@ def run_ours(args) -> None:
     if w.op not in ("encode+gather", "encode+decode", "stream+gather"):
         raise SystemExit(f"workload {cfg} ({w.op}) is not timed by bench.py")
     streaming = w.op == "stream+gather"
+    gathers = w.op != "encode+decode"            # encode+decode workloads decode every row
     C, Pi = pcb.for_workload(cfg)
     ctx = fq.fq_codebook_load(C, Pi, local)
     R = fq.fq_record_bits(ctx)
-    M, d = w.rows, w.d
-    # encode+decode workloads decode every row: a gather of all rows in order
-    gathers = w.op != "encode+decode"
+    M, d, nt = w.rows, w.d, w.tensors
+    # K and V share the codebook and rotation, so they share one code store: rows [t*M, (t+1)*M)
+    # hold tensor t. One encode launch covers all tensors, one decode launch all decoded rows.
+    MT = nt * M
     if streaming:
-        # (layer, head) sequences of capacity T; each step appends `new` tokens to every sequence.
-        n_seq, T, new = w.rows // w.shape[-2], w.shape[-2], w.stream_new
+        # (layer, head) sequences of capacity T per tensor; each append adds `new` tokens to all.
+        n_seq, T, new = M // w.shape[-2], w.shape[-2], w.stream_new
         n_steps = T // new
         pos = synth.token_positions(cfg, T, w.gather)
-        gidx = torch.from_numpy((np.arange(n_seq)[:, None] * T + pos[None, :]).reshape(-1).astype(np.int64))
-        G = int(gidx.numel())
+        per = (np.arange(n_seq)[:, None] * T + pos[None, :]).reshape(-1)
+        idx_np = np.concatenate([t * M + per for t in range(nt)]).astype(np.int64)
 
-        def arrival_order(a):  # [n_seq*T, d] -> [steps, n_seq*new, d], the order tokens arrive in
-            return np.ascontiguousarray(a.reshape(n_seq, n_steps, new, d).transpose(1, 0, 2, 3)).reshape(
-                n_steps, n_seq * new, d)
-        x_host = [torch.from_numpy(arrival_order(synth.kv_tensor(cfg, t))).pin_memory() for t in range(w.tensors)]
-        i_host = [gidx.pin_memory() for _ in range(w.tensors)]
+        def arrival_order(a):  # [n_seq*T, d] -> [steps, n_seq, new, d], the order tokens arrive in
+            return np.ascontiguousarray(a.reshape(n_seq, n_steps, new, d).transpose(1, 0, 2, 3))
+        x_np = np.concatenate([arrival_order(synth.kv_tensor(cfg, t)) for t in range(nt)], axis=1)
+        x_np = x_np.reshape(n_steps, nt * n_seq * new, d)
     else:
-        G = w.gather if gathers else M
-        x_host = [torch.from_numpy(synth.kv_tensor(cfg, t)).pin_memory() for t in range(w.tensors)]
+        x_np = np.concatenate([synth.kv_tensor(cfg, t) for t in range(nt)])
         if gathers:
-            i_host = [torch.from_numpy(synth.gather_indices(cfg, t, M, G)).pin_memory() for t in range(w.tensors)]
+            idx_np = np.concatenate([t * M + synth.gather_indices(cfg, t, M, w.gather) for t in range(nt)])
         else:
-            i_host = [torch.arange(M, dtype=torch.int64).pin_memory() for _ in range(w.tensors)]
-    xs = [h.to(dev) for h in x_host]
-    idxs = [h.to(dev) for h in i_host]
-    stores = [fq.alloc_store(ctx, M, dev) for _ in range(w.tensors)]
-    outs = [torch.empty((G, d), dtype=torch.float16, device=dev) for _ in range(w.tensors)]
+            idx_np = np.arange(MT, dtype=np.int64)
+    G = int(idx_np.size)
+    x_host = torch.from_numpy(x_np).pin_memory()
+    i_host = torch.from_numpy(idx_np).pin_memory()
+    xs = x_host.to(dev)
+    idx = i_host.to(dev)
+    nu, codes = fq.alloc_store(ctx, MT, dev)
+    out = torch.empty((G, d), dtype=torch.float16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
+    enc_launches = n_steps if streaming else 1
+    launches_per_step = enc_launches + 1
 
     def step(ev=None):
-        for t in range(w.tensors):
-            nu, codes = stores[t]
-            if ev is not None:
-                ev[f"enc{t}"][0].record(stream)
-            if streaming:
-                for st in range(n_steps):
-                    fq.fq_encode_append(ctx, xs[t][st], n_seq, new, T, st * new, nu, codes, sp)
-            else:
-                fq.fq_encode(ctx, xs[t], M, nu, codes, 0, sp)
-            if ev is not None:
-                ev[f"enc{t}"][1].record(stream)
-        for t in range(w.tensors):
-            nu, codes = stores[t]
-            if ev is not None:
-                ev[f"gat{t}"][0].record(stream)
-            if gathers:
-                fq.fq_decode_gather(ctx, nu, codes, M, idxs[t], G, outs[t], sp)
-            else:
-                fq.fq_decode(ctx, nu, codes, M, outs[t], sp)
-            if ev is not None:
-                ev[f"gat{t}"][1].record(stream)
+        if ev is not None:
+            ev[0].record(stream)
+        if streaming:
+            for st in range(n_steps):
+                fq.fq_encode_append(ctx, xs[st], nt * n_seq, new, T, st * new, nu, codes, sp)
+        else:
+            fq.fq_encode(ctx, xs, MT, nu, codes, 0, sp)
+        if ev is not None:
+            ev[1].record(stream)
+        if gathers:
+            fq.fq_decode_gather(ctx, nu, codes, MT, idx, G, out, sp)
+        else:
+            fq.fq_decode(ctx, nu, codes, MT, out, sp)
+        if ev is not None:
+            ev[2].record(stream)
 
-    enc_launches = n_steps if streaming else 1
-    launches_per_step = w.tensors * (enc_launches + 1)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
         step()
@@ -291,9 +289,7 @@ def run_ours(args) -> None:
     if fq.fq_status(ctx, sp) != 0:
         raise SystemExit("device flags set during warm-up")
 
-    names = [f"enc{t}" for t in range(w.tensors)] + [f"gat{t}" for t in range(w.tensors)]
-    per_step = []
-    kern = {n: [] for n in names}
+    evs = []
     sampler = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
@@ -301,20 +297,16 @@ def run_ours(args) -> None:
     sampler.start()
     for _ in range(args.steps):
         flush.zero_()
-        ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s0.record(stream)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         step(ev)
-        s1.record(stream)
-        per_step.append((s0, s1, ev))
+        evs.append(ev)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    step_ms = [a.elapsed_time(b) for a, b, _ in per_step]
-    for _, _, ev in per_step:
-        for n in names:
-            kern[n].append(ev[n][0].elapsed_time(ev[n][1]))
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    enc_step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_step_ms = [e[1].elapsed_time(e[2]) for e in evs]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -322,25 +314,23 @@ def run_ours(args) -> None:
         total_ms = float(t.item())
     flags = fq.fq_status(ctx, sp)
 
-    vec_per_step = w.tensors * (M + G)
+    vec_per_step = MT + G
     value = world * vec_per_step * args.steps / (total_ms / 1e3)
 
     # End to end through the public API from pinned host memory: H2D of the inputs, encode,
-    # gather, D2H of the codes, norms and decoded rows, every step.
-    nu_host = [torch.empty(M, dtype=torch.float32).pin_memory() for _ in range(w.tensors)]
-    code_host = [torch.empty_like(stores[t][1], device="cpu").pin_memory() for t in range(w.tensors)]
-    out_host = [torch.empty((G, d), dtype=torch.float16).pin_memory() for _ in range(w.tensors)]
+    # decode, D2H of the codes, norms and decoded rows, every step.
+    nu_host = torch.empty_like(nu, device="cpu").pin_memory()
+    code_host = torch.empty_like(codes, device="cpu").pin_memory()
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
 
     def e2e_step():
-        for t in range(w.tensors):
-            xs[t].copy_(x_host[t], non_blocking=True)
-            if gathers:
-                idxs[t].copy_(i_host[t], non_blocking=True)
+        xs.copy_(x_host, non_blocking=True)
+        if gathers:
+            idx.copy_(i_host, non_blocking=True)
         step()
-        for t in range(w.tensors):
-            nu_host[t].copy_(stores[t][0], non_blocking=True)
-            code_host[t].copy_(stores[t][1], non_blocking=True)
-            out_host[t].copy_(outs[t], non_blocking=True)
+        nu_host.copy_(nu, non_blocking=True)
+        code_host.copy_(codes, non_blocking=True)
+        out_host.copy_(out, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -354,8 +344,8 @@ def run_ours(args) -> None:
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    h2d = sum(x.numel() * 2 + (i.numel() * 8 if gathers else 0) for x, i in zip(x_host, i_host))
-    d2h = sum(n.numel() * 4 + c.numel() * 4 + o.numel() * 2 for n, c, o in zip(nu_host, code_host, out_host))
+    h2d = x_host.numel() * 2 + (i_host.numel() * 8 if gathers else 0)
+    d2h = nu_host.numel() * 4 + code_host.numel() * 4 + out_host.numel() * 2
     e2e_total = sum(e2e_ms)
     if world > 1:
         t = torch.tensor([e2e_total], device=dev)
@@ -366,20 +356,21 @@ def run_ours(args) -> None:
     enc_b, gat_b = workload_bytes(w, R)
     if not gathers:
         gat_b -= 8                          # a full decode reads no index array
-    # per launch: a streamed encode is n_steps append launches of M / n_steps rows each
-    enc_ms = statistics.mean(kern["enc0"] + kern.get("enc1", [])) / enc_launches
-    enc_rows = M // enc_launches
-    gat_ms = statistics.mean(kern["gat0"] + kern.get("gat1", []))
+    # per launch: a streamed encode is n_steps append launches of MT / n_steps rows each
+    enc_ms = statistics.mean(enc_step_ms) / enc_launches
+    enc_rows = MT // enc_launches
+    gat_ms = statistics.mean(dec_step_ms)
     peaks = measured_peaks()
     dec_name = "decode_gather" if gathers else "decode"
-    if enc_ms * enc_launches * M >= gat_ms * G * enc_launches:
+    if enc_ms * enc_launches >= gat_ms:
         dom, dom_bytes, dom_ms = "encode", enc_b * enc_rows, enc_ms
         kname = "fq_encode_append" if streaming else "fq_encode"
     else:
         dom, dom_bytes, dom_ms, kname = dec_name, gat_b * G, gat_ms, "fq_" + dec_name
     roofline = {"kernel": dom, "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": int(dom_bytes), "launch_ms": round(dom_ms, 5),
-                "encode_launch_ms": round(enc_ms, 5), f"{dec_name}_launch_ms": round(gat_ms, 5),
+                "encode_launch_ms": round(enc_ms, 5), "encode_rows_per_launch": enc_rows,
+                f"{dec_name}_launch_ms": round(gat_ms, 5), f"{dec_name}_rows_per_launch": G,
                 "encode_gbs": round(enc_b * enc_rows / (enc_ms / 1e3) / 1e9, 1),
                 f"{dec_name}_gbs": round(gat_b * G / (gat_ms / 1e3) / 1e9, 1)}
     if dom == "encode" and w.k == w.d:
@@ -401,17 +392,20 @@ def run_ours(args) -> None:
                "sample": r["sample"], "seconds": round(r["seconds"], 2)}
 
     if rank == 0:
+        conf = {"workload": w.name, "rows_per_tensor": M, "tensors": nt, "d": d, "k": w.k, "N": w.N,
+                "bits_per_coordinate": w.B / w.k, "record_bits": R,
+                ("gathered_rows" if gathers else "decoded_rows"): G,
+                "layout": "K and V in one code store; one encode and one decode launch per step"
+                          + (" (one append launch per token block)" if streaming else ""),
+                "l2": "flushed before every timed step (256 MB write, outside the step events)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+        if streaming:
+            conf.update({"append_steps": n_steps, "tokens_per_append": new, "sequences": nt * n_seq})
         line = {
             "metric": METRIC, "value": value, "unit": "vectors/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name, "rows_per_tensor": M, "tensors": w.tensors, "d": d, "k": w.k,
-                       "N": w.N, "bits_per_coordinate": w.B / w.k, "record_bits": R,
-                       ("gather_per_tensor" if gathers else "decoded_per_tensor"): G,
-                       **({"append_steps": n_steps, "tokens_per_append": new, "sequences": n_seq}
-                          if streaming else {}),
-                       "l2": "flushed before every timed step (256 MB write, outside the step events)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": conf,
             "fp16_gbps": value * 2 * d / 1e9,
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -42,6 +42,7 @@ constexpr int kOvfMax = 12;
 constexpr int kCellBytes = (kGridR * kGridR * 4 + 15) & ~15;
 constexpr float kMagic = 12582912.f;       // 1.5 * 2^23: adding it rounds to an integer held in the low bits
 constexpr int kMagicBits = 0x4B400000;
+constexpr int kCluster = 4;                // CTAs that share one L2 read of the tables (multicast)
 
 template <int D, int NG, int NBUF>
 struct Layout {
@@ -53,7 +54,7 @@ struct Layout {
     static constexpr int oOvf = oGrid + kCellBytes;
     static constexpr int oCw = oOvf + kOvfSlots * 16;
     static constexpr int oBar = oCw + 256 * 8;
-    static constexpr int kBars = 1 + NG * NBUF + NG;
+    static constexpr int kBars = 2 + NG * NBUF + NG;
     static constexpr int oTmem = oBar + kBars * 8;
     static constexpr int kBytes = oTmem + 16 + 1024;             // + alignment slack
     static constexpr uint32_t kTmemCols = (NG * D <= 32) ? 32 : (NG * D <= 64) ? 64 : (NG * D <= 128) ? 128
@@ -102,12 +103,27 @@ __device__ __noinline__ uint32_t marked_cell(float u0, float u1, uint32_t e, con
     return bi;
 }
 
-// Candidate scoring of one block by squared difference. Returns the index; sets `marked` for
-// marker cells (first byte above last byte: impossible for a real entry, whose bytes ascend and
-// are padded with the first). Candidates are 8-byte codeword loads, issued only for distinct
-// entries, so a single-candidate cell reads no codeword at all.
+// Loads the float2 at shared address `addr` into v when p holds; otherwise v keeps its value.
+// Predicated rather than branched, so that the blocks of a chunk stay independent instruction
+// streams, and lanes that skip the load issue no shared-memory wavefront.
+__device__ __forceinline__ void ld_shared_f2_if(bool p, uint32_t addr, float2 &v) {
+    asm("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %3, 0;\n\t@q ld.shared.v2.f32 {%0, %1}, [%2];\n\t}"
+        : "+f"(v.x), "+f"(v.y)
+        : "r"(addr), "r"((uint32_t)p));
+}
+
+__device__ __forceinline__ float sqdiff(float u0, float u1, float2 c) {
+    const float e0 = u0 - c.x, e1 = u1 - c.y;
+    return fmaf(e1, e1, e0 * e0);
+}
+
+// Candidate scoring of one block by squared difference, branch-free. Returns the index; sets
+// `marked` for marker cells (first byte above last byte: impossible for a real entry, whose bytes
+// ascend and are padded with the first). A padded slot repeats the first candidate, so its load is
+// skipped and its score equals the first one, which a strict comparison never prefers; a
+// single-candidate cell reads no codeword at all.
 __device__ __forceinline__ uint32_t fast_block(float a0, float a1, float s, float sg, float gom,
-                                               const uint32_t *grid, const float2 *cw, uint32_t &e_out,
+                                               const uint32_t *grid, uint32_t cw_base, uint32_t &e_out,
                                                bool &marked) {
     const float lo = kMagic, hi = kMagic + (float)(kGridR - 1);
     const float gx = fminf(fmaxf(fmaf(a0, sg, gom), lo), hi);
@@ -118,15 +134,20 @@ __device__ __forceinline__ uint32_t fast_block(float a0, float a1, float s, floa
     const float u0 = a0 * s, u1 = a1 * s;
     const uint32_t b0 = e & 0xFFu, b1 = (e >> 8) & 0xFFu, b2 = (e >> 16) & 0xFFu, b3 = e >> 24;
     marked = b0 > b3;
+    float2 c0 = make_float2(0.f, 0.f);
+    ld_shared_f2_if(b1 != b0, cw_base + 8u * b0, c0);
+    float2 c1 = c0, c2 = c0, c3 = c0;
+    ld_shared_f2_if(b1 != b0, cw_base + 8u * b1, c1);
+    ld_shared_f2_if(b2 != b0, cw_base + 8u * b2, c2);
+    ld_shared_f2_if(b3 != b0, cw_base + 8u * b3, c3);
+    float best = sqdiff(u0, u1, c0);
     uint32_t bi = b0;
-    if (b1 != b0) {
-        const float2 c0 = cw[b0];
-        const float d00 = u0 - c0.x, d01 = u1 - c0.y;
-        float best = fmaf(d01, d01, d00 * d00);
-        diff_score(u0, u1, cw[b1], b1, best, bi);
-        if (b2 != b0) diff_score(u0, u1, cw[b2], b2, best, bi);
-        if (b3 != b0) diff_score(u0, u1, cw[b3], b3, best, bi);
-    }
+    const float s1 = sqdiff(u0, u1, c1), s2 = sqdiff(u0, u1, c2), s3 = sqdiff(u0, u1, c3);
+    bi = s1 < best ? b1 : bi;
+    best = fminf(best, s1);
+    bi = s2 < best ? b2 : bi;
+    best = fminf(best, s2);
+    bi = s3 < best ? b3 : bi;
     return bi;
 }
 
@@ -144,15 +165,15 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     uint4 *ovf = reinterpret_cast<uint4 *>(sm + L::oOvf);
     float2 *cw = reinterpret_cast<float2 *>(sm + L::oCw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
-    uint64_t *bar_tab = bars;
+    uint64_t *bar_pi = bars, *bar_grid = bars + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
 
     const int tid = threadIdx.x;
     const int g = tid / 128;              // row group
     const int t = tid % 128;              // row within the tile = TMEM lane
     const int wq = t / 32;                // lane quarter of this warp
-    uint64_t *bar_load = bars + 1 + g * NBUF;
-    uint64_t *bar_mma = bars + 1 + NG * NBUF + g;
+    uint64_t *bar_load = bars + 2 + g * NBUF;
+    uint64_t *bar_mma = bars + 2 + NG * NBUF + g;
     uint8_t *xbuf0 = sm + L::oX + (g * NBUF) * L::kXTile;
 
     const int64_t ntiles = (p.M + kTileRows - 1) / kTileRows;
@@ -168,14 +189,28 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // Shared tables: the cluster's CTAs each fetch a slice and multicast it to all of them, so the
+    // cluster reads them from L2 once. Pi has its own barrier so that the first rotation can start
+    // while the candidate grid is still arriving.
+    cluster_sync();                                   // every CTA's barriers are initialised
     if (tid == 0) {
         prefetch_tensormap(&xmap);
         const uint32_t cw_bytes = (uint32_t)p.N * 8u;
         const uint32_t tab_bytes = kCellBytes + kOvfSlots * 16u;
-        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + tab_bytes + cw_bytes);
-        bulk_g2s(pi, p.pi_split, 2u * L::kPiPart, bar_tab);
-        bulk_g2s(grid, p.tables, tab_bytes, bar_tab);
-        bulk_g2s(cw, p.cw, cw_bytes, bar_tab);
+        mbar_arrive_expect_tx(bar_pi, 2u * L::kPiPart);
+        mbar_arrive_expect_tx(bar_grid, tab_bytes + cw_bytes);
+        const uint32_t r = cluster_ctarank();
+        const uint16_t all = (uint16_t)((1u << kCluster) - 1u);
+        auto slice = [&](void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+            const uint32_t per = ((bytes + kCluster - 1) / kCluster + 15u) & ~15u;
+            const uint32_t a = r * per, b = (a + per < bytes) ? a + per : bytes;
+            if (a < b)
+                bulk_g2s_multicast(static_cast<uint8_t *>(dst) + a, static_cast<const uint8_t *>(src) + a, b - a, bar,
+                                   all);
+        };
+        slice(pi, p.pi_split, 2u * L::kPiPart, bar_pi);
+        slice(grid, p.tables, tab_bytes, bar_grid);
+        slice(cw, p.cw, cw_bytes, bar_grid);
     }
     // Each row group's first x tile.
     if (t == 0 && first < ntiles) {
@@ -184,7 +219,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         for (int kb = 0; kb < D / 64; ++kb)
             tma_load_2d(xbuf0 + kb * 16384, &xmap, kb * 64, (int)(first * kTileRows), bar_load);
     }
-    bool ok = named_sync_and(1 + g, 128, mbar_wait(bar_tab, 0));
+    bool ok = named_sync_and(1 + g, 128, mbar_wait(bar_pi, 0));
 
     const uint32_t idesc = idesc_f16_f32(128, D);
     const uint32_t tmem_acc = tmem_base + (uint32_t)(g * D);
@@ -192,6 +227,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     const int R = (D / 2) * p.B;
     // +1: cell (i, j) sits at (i+1, j+1) inside the ring. goffs is an integer, so this is exact.
     const float gom = p.goffs + 1.0f + kMagic;
+    const uint32_t cw_base = smem_addr(cw);
 
     int64_t it = 0;
     for (int64_t tile = first; tile < ntiles && ok; tile += gstride, ++it) {
@@ -241,7 +277,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
                 }
             }
         }
-        ok = named_sync_and(1 + g, 128, mbar_wait(bar_mma, (uint32_t)(it & 1)));
+        ok = named_sync_and(1 + g, 128, mbar_wait(bar_mma, (uint32_t)(it & 1)) && (it > 0 || mbar_wait(bar_grid, 0)));
         if (!ok) break;
         tc_fence_after();
 
@@ -269,7 +305,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 bool m;
-                idx[j] = fast_block(a[2 * j], a[2 * j + 1], s, sg, gom, grid, cw, ent[j], m);
+                idx[j] = fast_block(a[2 * j], a[2 * j + 1], s, sg, gom, grid, cw_base, ent[j], m);
                 marks |= (uint32_t)m << j;
             }
             if (marks && live && !zero) {
@@ -324,6 +360,8 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         }
     }
     if (!ok && t == 0) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+    // A CTA without tiles still waits for the tables, so that nothing is in flight into it.
+    if (it == 0) mbar_wait(bar_grid, 0);
     __syncthreads();
     if (!ok) {
         // Give in-flight copies and MMAs a bounded chance to land before the CTA's memory goes away.
@@ -332,6 +370,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     }
     tc_fence_after();
     if (tid < 32) tmem_dealloc(tmem_base, L::kTmemCols);
+    cluster_sync();                                   // no multicast from a peer is still landing
 }
 
 template <int D, int NG, int NBUF, int BS>
@@ -355,28 +394,59 @@ cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     p.flags = ctx->flags;
     const int64_t ntiles = (M + kTileRows - 1) / kTileRows;
     int64_t grid = (ntiles + NG - 1) / NG;
-    if (grid > ctx->num_sms) grid = ctx->num_sms;
-    encode_k2_tc<D, NG, NBUF, BS><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(tm, p);
-    return cudaGetLastError();
+    if (grid > ctx->k2_max_ctas) grid = ctx->k2_max_ctas;
+    grid = (grid + kCluster - 1) / kCluster * kCluster;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NG * 128);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, encode_k2_tc<D, NG, NBUF, BS>, tm, p);
 }
 
 template <int D, int NG, int NBUF, int BS>
-cudaError_t prep_k2() {
+cudaError_t prep_k2(fq_ctx *ctx) {
     using L = Layout<D, NG, NBUF>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
-    return cudaFuncSetAttribute(encode_k2_tc<D, NG, NBUF, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                L::kBytes);
+    cudaError_t e = cudaFuncSetAttribute(encode_k2_tc<D, NG, NBUF, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kBytes);
+    if (e != cudaSuccess) return e;
+    // The persistent grid: as many clusters as can be resident at once.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(ctx->num_sms / kCluster * kCluster));
+    cfg.blockDim = dim3(NG * 128);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, encode_k2_tc<D, NG, NBUF, BS>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    ctx->k2_max_ctas = clusters * kCluster;
+    return cudaSuccess;
 }
 
 // Static packing when B divides 32 (B = 1, 2, 4, 8); the generic bit writer otherwise.
 template <int D, int NG, int NBUF>
-cudaError_t dispatch_prep(int B) {
-    switch (B) {
-        case 1: return prep_k2<D, NG, NBUF, 1>();
-        case 2: return prep_k2<D, NG, NBUF, 2>();
-        case 4: return prep_k2<D, NG, NBUF, 4>();
-        case 8: return prep_k2<D, NG, NBUF, 8>();
-        default: return prep_k2<D, NG, NBUF, 0>();
+cudaError_t dispatch_prep(fq_ctx *ctx) {
+    switch (ctx->B) {
+        case 1: return prep_k2<D, NG, NBUF, 1>(ctx);
+        case 2: return prep_k2<D, NG, NBUF, 2>(ctx);
+        case 4: return prep_k2<D, NG, NBUF, 4>(ctx);
+        case 8: return prep_k2<D, NG, NBUF, 8>(ctx);
+        default: return prep_k2<D, NG, NBUF, 0>(ctx);
     }
 }
 
@@ -522,8 +592,8 @@ cudaError_t prepare_k2_tc(fq_ctx *ctx) {
     if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->pi_split, pis.size() * 2);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->pi_split, pis.data(), pis.size() * 2, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return e;
-    if (ctx->d == 64) return dispatch_prep<64, 4, 2>(ctx->B);
-    return dispatch_prep<128, 2, 1>(ctx->B);
+    if (ctx->d == 64) return dispatch_prep<64, 4, 2>(ctx);
+    return dispatch_prep<128, 2, 1>(ctx);
 }
 
 cudaError_t launch_encode_k2_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,

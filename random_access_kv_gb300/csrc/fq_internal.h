@@ -23,6 +23,7 @@ struct fq_ctx {
     uint8_t *pi_split;           // fp16 halves of 2^12 Pi, swizzled as the MMA's B operand
     uint32_t *grid2;             // candidate grid and overflow slots
     float g_scale, g_offs;       // grid cell of u: round(u * g_scale + g_offs)
+    int k2_max_ctas;             // co-resident CTAs of the k = 2 encoder (whole clusters)
     // tensor-core decoder tables
     uint8_t *pit_split;          // fp16 halves of 2^12 Pi^T, swizzled as the MMA's B operand
     uint16_t *cb_split;          // [N][2k] fp16 halves of 2^10 c_n (k hi, then k lo)

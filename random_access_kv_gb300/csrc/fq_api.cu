@@ -48,6 +48,7 @@ void free_ctx(fq_ctx *c) {
     cudaFree(c->pit_split);
     cudaFree(c->cb_split);
     cudaFree(c->crot_split);
+    cudaFree(c->cb_ops);
     free(c);
 }
 
@@ -144,6 +145,7 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
     if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
     if (e == cudaSuccess && is_full(c) && fq::full_tc_supported(c)) e = fq::prepare_full_tc(c);
+    if (e == cudaSuccess && !is_full(c) && !c->grid2 && fq::kq_tc_supported(c)) e = fq::prepare_kq_tc(c);
     if (e != cudaSuccess) {
         const int rc = (e == cudaErrorMemoryAllocation) ? FQ_ENOMEM : FQ_ECUDA;
         free_ctx(c);
@@ -183,8 +185,10 @@ static int encode_common(fq_ctx *ctx, const void *x, int64_t M, fq::RowMap map, 
         e = fq::launch_encode_full_tc(ctx, (const __half *)x, M, map, nu, codes, s);
     else if (is_full(ctx))
         e = fq::launch_encode_full(ctx, (const __half *)x, M, map, nu, codes, s);
-    else if (ctx->pi_split)
+    else if (ctx->grid2)
         e = fq::launch_encode_k2_tc(ctx, (const __half *)x, M, map, nu, codes, s);
+    else if (ctx->cb_ops)
+        e = fq::launch_encode_kq_tc(ctx, (const __half *)x, M, map, nu, codes, s);
     else
         e = fq::launch_encode_blocks(ctx, (const __half *)x, M, map, nu, codes, s);
     return e == cudaSuccess ? FQ_OK : FQ_ECUDA;

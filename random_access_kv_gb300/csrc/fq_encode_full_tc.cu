@@ -173,35 +173,41 @@ encode_full_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
                 mphase ^= 1;
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll 1
-                for (int c = 0; c < kNT / 16; ++c) {
-                    float a[16];
-                    tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), a);
+                // Two halves of 64 columns: four 32-column loads in flight per wait.
+#pragma unroll
+                for (int hh = 0; hh < kNT / 64; ++hh) {
+                    uint32_t r[2][32];
+                    tmem_ld32_nowait(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(64 * hh), r[0]);
+                    tmem_ld32_nowait(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(64 * hh + 32), r[1]);
                     tmem_wait_ld();
-                    const int n0 = bt * kNT + c * 16;
-                    const float4 *h4 = reinterpret_cast<const float4 *>(hs + n0);
-                    float sc[16];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 hv = h4[q];
-                        sc[4 * q + 0] = fmaf(a[4 * q + 0], rs, hv.x);
-                        sc[4 * q + 1] = fmaf(a[4 * q + 1], rs, hv.y);
-                        sc[4 * q + 2] = fmaf(a[4 * q + 2], rs, hv.z);
-                        sc[4 * q + 3] = fmaf(a[4 * q + 3], rs, hv.w);
-                    }
-                    float m8[8];
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t *a = &r[c / 2][16 * (c % 2)];
+                        const int n0 = bt * kNT + hh * 64 + c * 16;
+                        const float4 *h4 = reinterpret_cast<const float4 *>(hs + n0);
+                        float sc[16];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) m8[q] = fminf(sc[2 * q], sc[2 * q + 1]);
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 hv = h4[q];
+                            sc[4 * q + 0] = fmaf(__uint_as_float(a[4 * q + 0]), rs, hv.x);
+                            sc[4 * q + 1] = fmaf(__uint_as_float(a[4 * q + 1]), rs, hv.y);
+                            sc[4 * q + 2] = fmaf(__uint_as_float(a[4 * q + 2]), rs, hv.z);
+                            sc[4 * q + 3] = fmaf(__uint_as_float(a[4 * q + 3]), rs, hv.w);
+                        }
+                        float m8[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) m8[q] = fminf(m8[2 * q], m8[2 * q + 1]);
-                    const float cmin = fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3]));
-                    if (cmin < best) {
-                        best = cmin;
-                        uint32_t j = 15;
+                        for (int q = 0; q < 8; ++q) m8[q] = fminf(sc[2 * q], sc[2 * q + 1]);
 #pragma unroll
-                        for (int q = 15; q >= 0; --q)
-                            if (sc[q] == cmin) j = (uint32_t)q;
-                        bi = (uint32_t)n0 + j;
+                        for (int q = 0; q < 4; ++q) m8[q] = fminf(m8[2 * q], m8[2 * q + 1]);
+                        const float cmin = fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3]));
+                        if (cmin < best) {
+                            best = cmin;
+                            uint32_t j = 15;
+#pragma unroll
+                            for (int q = 15; q >= 0; --q)
+                                if (sc[q] == cmin) j = (uint32_t)q;
+                            bi = (uint32_t)n0 + j;
+                        }
                     }
                 }
                 tc_fence_before();

@@ -29,6 +29,9 @@ struct fq_ctx {
     uint16_t *cb_split;          // [N][2k] fp16 halves of 2^10 c_n (k hi, then k lo)
     // k = d tensor-core encoder table
     uint16_t *crot_split;        // [2][N x d] fp16 halves of -2 * 2^12 Crot (hi block, then lo block)
+    // k = 4, 8 tensor-core encoder table
+    uint8_t *cb_ops;             // codebook rows as MMA B operands (see fq_encode_kq.cu)
+    int kq_max_ctas;
 };
 
 namespace fq {
@@ -73,6 +76,10 @@ bool full_tc_supported(const fq_ctx *ctx);
 cudaError_t prepare_full_tc(fq_ctx *ctx);
 cudaError_t launch_encode_full_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                   uint32_t *codes, cudaStream_t s);
+bool kq_tc_supported(const fq_ctx *ctx);
+cudaError_t prepare_kq_tc(fq_ctx *ctx);
+cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
+                                uint32_t *codes, cudaStream_t s);
 // One-time kernel attribute set-up (dynamic shared memory limits); called by fq_codebook_load.
 cudaError_t prepare_encode_blocks(const fq_ctx *ctx);
 cudaError_t prepare_decode_blocks(const fq_ctx *ctx);

@@ -40,8 +40,9 @@ using namespace sm100;
 constexpr int kRows = 128;
 constexpr int kStages = 4;
 constexpr int kCQ = 4;                    // consumer warps per lane quarter (column quarters of an item)
+constexpr int kSB = 3;                    // TMEM score buffers (MMAs in flight ahead of the readers)
 constexpr int kConsumerWarps = 4 * kCQ;
-constexpr int kThreads = kConsumerWarps * 32 + 32;      // + the producer warp
+constexpr int kThreads = kConsumerWarps * 32 + 64;      // + the loader warp and the MMA warp
 constexpr float kPiScale = 4096.f;        // 2^12 on Pi
 constexpr float kOpScale = 1024.f;        // 2^10 on u, -2c and |c|^2
 
@@ -61,14 +62,14 @@ struct KQ {
     static constexpr int oB = oA + NBH * kABlock;
     static constexpr int oState = oB + kStages * kBTile;         // per (block, quarter, row): best, index
     static constexpr int oBar = oState + NBH * kCQ * kRows * 8;
-    // bars: pi, x, rot, score[2], full[kStages], empty[kStages]
-    static constexpr int kBars = 5 + 2 * kStages;
+    // bars: pi, x, rot, a_ready, rot_free, ready[kSB], free[kSB], full[kStages], empty[kStages]
+    static constexpr int kBars = 5 + 2 * kSB + 2 * kStages;
     static constexpr int oTmem = oBar + kBars * 8;
     static constexpr int kBytes = oTmem + 16 + 1024;
-    // TMEM: two score buffers of kNT columns; the rotation lives past them when it must survive
-    // the first pass.
-    static constexpr int kRotCol = NPASS > 1 ? 2 * kNT : 0;
-    static constexpr int kCols = kRotCol + (NPASS > 1 ? D : (D > 2 * kNT ? D : 2 * kNT));
+    // TMEM: kSB score buffers of kNT columns, then the rotation (so that the next tile's rotation
+    // can run while the last scores are read).
+    static constexpr int kRotCol = kSB * kNT;
+    static constexpr int kCols = kRotCol + D;
     static constexpr uint32_t kTmemCols = kCols <= 256 ? 256 : 512;
     static_assert(kCols <= 512, "tensor memory");
 };
@@ -106,8 +107,10 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
-    uint64_t *bar_pi = bars, *bar_x = bars + 1, *bar_rot = bars + 2, *bar_s = bars + 3;
-    uint64_t *full = bars + 5, *empty = bars + 5 + kStages;
+    uint64_t *bar_pi = bars + 0, *bar_x = bars + 1, *bar_rot = bars + 2;
+    uint64_t *a_ready = bars + 3, *rot_free = bars + 4;
+    uint64_t *ready = bars + 5, *freeb = bars + 5 + kSB;              // [kSB] each
+    uint64_t *full = bars + 5 + 2 * kSB, *empty = bars + 5 + 2 * kSB + kStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
     uint8_t *xt = sm + L::oX;
     float *st_best = reinterpret_cast<float *>(sm + L::oState);
@@ -115,11 +118,21 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
 
     const int tid = threadIdx.x;
     const int warp = tid / 32;
+    const int lane = tid & 31;
     const int64_t ntiles = (p.M + kRows - 1) / kRows;
     const int nbt = p.N / kNT;
+    constexpr uint32_t kCons = kConsumerWarps * 32;
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) mbar_init(bars + i, 1);
+        mbar_init(bar_pi, 1);
+        mbar_init(bar_x, 1);
+        mbar_init(bar_rot, 1);
+        mbar_init(a_ready, kConsumerWarps);
+        mbar_init(rot_free, kConsumerWarps);
+        for (int b = 0; b < kSB; ++b) {
+            mbar_init(ready + b, 1);
+            mbar_init(freeb + b, kConsumerWarps);
+        }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
@@ -130,10 +143,20 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const uint32_t rot_acc = tmem_base + (uint32_t)L::kRotCol;
 
     if (warp == kConsumerWarps) {
-        // Producer: the codebook tiles, in the order the consumers use them.
-        if ((tid & 31) == 0) {
+        // Loader: Pi, the first x tile, then the codebook tiles in the order they are used.
+        if (lane == 0) {
+            prefetch_tensormap(&xmap);
+            mbar_arrive_expect_tx(bar_pi, 2u * L::kPiPart);
+            bulk_g2s(sm + L::oPi, p.pi_split, 2u * L::kPiPart, bar_pi);
+            if ((int64_t)blockIdx.x < ntiles) {
+                mbar_arrive_expect_tx(bar_x, (uint32_t)L::kXTile);
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb)
+                    tma_load_2d(xt + kb * 16384, &xmap, kb * 64, (int)(blockIdx.x * kRows), bar_x);
+            }
             uint32_t k = 0;
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x)
@@ -147,39 +170,21 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     }
             if (!ok) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
         }
-    } else {
-        // Consumers: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows) and column quarter w / 4
-        // of every score item.
-        const int lq = warp % 4, cq = warp / 4;
-        const int t = 32 * lq + (tid & 31);        // row within the tile = TMEM lane
-        const bool lead = tid == 0;
-        constexpr uint32_t kCons = kConsumerWarps * 32;
-        if (lead) {
-            prefetch_tensormap(&xmap);
-            mbar_arrive_expect_tx(bar_pi, 2u * L::kPiPart);
-            bulk_g2s(sm + L::oPi, p.pi_split, 2u * L::kPiPart, bar_pi);
-            if ((int64_t)blockIdx.x < ntiles) {
-                mbar_arrive_expect_tx(bar_x, (uint32_t)L::kXTile);
-#pragma unroll
-                for (int kb = 0; kb < D / 64; ++kb)
-                    tma_load_2d(xt + kb * 16384, &xmap, kb * 64, (int)(blockIdx.x * kRows), bar_x);
-            }
-        }
-        bool ok = named_sync_and(1, kCons, mbar_wait(bar_pi, 0));
-        const uint32_t idesc_rot = idesc_f16_f32(128, D);
-        const uint32_t idesc_sc = idesc_f16_f32(128, kNT);
-        const uint32_t pi_hi = smem_addr(sm + L::oPi), pi_lo = pi_hi + L::kPiPart;
-        const uint32_t a_base = smem_addr(sm + L::oA), b_base = smem_addr(sm + L::oB);
-        const uint32_t rot_acc = tmem_base + (uint32_t)L::kRotCol;
-        const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
-        const int R = L::NB * p.B;
-        uint32_t kq = 0;                   // codebook tiles consumed (ring position)
-        uint32_t sphase = 0u;              // bit b: phase parity of score buffer b
-        int64_t it = 0;
-        for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-            ok = named_sync_and(1, kCons, mbar_wait(bar_x, (uint32_t)(it & 1)));
-            if (!ok) break;
-            if (lead) {
+    } else if (warp == kConsumerWarps + 1) {
+        // MMA issuer: the rotation of each tile, then its score items in order.
+        if (lane == 0) {
+            const uint32_t idesc_rot = idesc_f16_f32(128, D);
+            const uint32_t idesc_sc = idesc_f16_f32(128, kNT);
+            const uint32_t pi_hi = smem_addr(sm + L::oPi), pi_lo = pi_hi + L::kPiPart;
+            const uint32_t a_base = smem_addr(sm + L::oA), b_base = smem_addr(sm + L::oB);
+            bool ok = mbar_wait(bar_pi, 0);
+            uint32_t k = 0, item = 0, npass = 0;
+            int64_t it = 0;
+            for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+                ok = mbar_wait(bar_x, (uint32_t)(it & 1));
+                // The consumers have read the previous tile's rotation.
+                if (ok && it > 0) ok = mbar_wait(rot_free, (uint32_t)((it - 1) & 1));
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t xa = smem_addr(xt);
 #pragma unroll
@@ -193,26 +198,66 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     }
                 }
                 mma_commit(bar_rot);
-            }
-            float ss = 0.f;
+                for (int pass = 0; pass < L::NPASS && ok; ++pass, ++npass) {
+                    ok = mbar_wait(a_ready, npass & 1);
+                    for (int bt = 0; bt < nbt && ok; ++bt, ++k) {
+                        const uint32_t s = k % kStages;
+                        ok = mbar_wait(full + s, (k / kStages) & 1);
+                        for (int bb = 0; bb < NBH && ok; ++bb, ++item) {
+                            const uint32_t buf = item % kSB;
+                            // Buffer `buf` was last filled by item - kSB; wait until it has been read.
+                            if (item >= kSB) ok = mbar_wait(freeb + buf, ((item - kSB) / kSB) & 1);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t aa = a_base + (uint32_t)(bb * L::kABlock);
+                            const uint32_t ba = b_base + s * (uint32_t)L::kBTile;
+                            const uint32_t dst = tmem_base + buf * (uint32_t)kNT;
 #pragma unroll
-            for (int kb = 0; kb < D / 64; ++kb) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xt + kb * 16384 + t * 128 + ((c ^ (t & 7)) << 4));
-                    const __half2 *h2 = reinterpret_cast<const __half2 *>(&v);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 f = __half22float2(h2[q]);
-                        ss = fmaf(f.x, f.x, ss);
-                        ss = fmaf(f.y, f.y, ss);
+                            for (int kk = 0; kk < KP / 16; ++kk)
+                                mma_f16(dst, sdesc_kmajor_noswz(aa + kk * 256, (KP / 8) * 128),
+                                        sdesc_kmajor_noswz(ba + kk * 256, (KP / 8) * 128), idesc_sc, kk ? 1u : 0u);
+                            mma_commit(ready + buf);
+                        }
+                        if (ok) mma_commit(empty + s);
                     }
                 }
             }
-            ok = named_sync_and(1, kCons, mbar_wait(bar_rot, (uint32_t)(it & 1)));
+            if (!ok) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+        }
+    } else {
+        // Consumers: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows) and column quarter w / 4
+        // of every score item.
+        const int lq = warp % 4, cq = warp / 4;
+        const int t = 32 * lq + lane;             // row within the tile = TMEM lane
+        const bool lead = tid == 0;
+        const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
+        const int R = L::NB * p.B;
+        uint32_t item = 0;
+        bool ok = true;
+        int64_t it = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
+            ok = mbar_wait(bar_x, (uint32_t)(it & 1));
+            float ss = 0.f;
+            if (ok) {
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(xt + kb * 16384 + t * 128 + ((c ^ (t & 7)) << 4));
+                        const __half2 *h2 = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = __half22float2(h2[q]);
+                            ss = fmaf(f.x, f.x, ss);
+                            ss = fmaf(f.y, f.y, ss);
+                        }
+                    }
+                }
+            }
+            ok = named_sync_and(1, kCons, ok && mbar_wait(bar_rot, (uint32_t)(it & 1)));
             if (!ok) break;
             tc_fence_after();
-            // The rotation has consumed the x tile: fetch the next one now.
+            // nu is read and the rotation has consumed the x tile: fetch the next one.
             const int64_t next = tile + gridDim.x;
             if (lead && next < ntiles) {
                 mbar_arrive_expect_tx(bar_x, (uint32_t)L::kXTile);
@@ -266,80 +311,71 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                ok = named_sync_and(1, kCons, true);
-                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(a_ready);
+                    if (pass == L::NPASS - 1) mbar_arrive(rot_free);
+                }
 
                 const int items = nbt * NBH;
-                // Issues the MMA of item i = (codebook tile i / NBH, block i % NBH) into score buffer i % 2.
-                auto issue = [&](int i) -> bool {
-                    const int bt = i / NBH, bb = i % NBH;
-                    const uint32_t k = kq + (uint32_t)bt, s = k % kStages;
-                    if (bb == 0 && !mbar_wait(full + s, (k / kStages) & 1)) return false;
-                    tc_fence_after();
-                    const uint32_t aa = a_base + (uint32_t)(bb * L::kABlock);
-                    const uint32_t ba = b_base + s * (uint32_t)L::kBTile;
-                    const uint32_t dst = tmem_base + (uint32_t)((i & 1) * kNT);
-#pragma unroll
-                    for (int kk = 0; kk < KP / 16; ++kk)
-                        mma_f16(dst, sdesc_kmajor_noswz(aa + kk * 256, (KP / 8) * 128),
-                                sdesc_kmajor_noswz(ba + kk * 256, (KP / 8) * 128), idesc_sc, kk ? 1u : 0u);
-                    mma_commit(bar_s + (i & 1));
-                    if (bb == NBH - 1) mma_commit(empty + s);
-                    return true;
-                };
-                bool iok = true;
-                if (lead) iok = issue(0);
 #pragma unroll 1
-                for (int i = 0; i < items; ++i) {
-                    if (lead && iok && i + 1 < items) iok = issue(i + 1);
-                    const int buf = i & 1, bt = i / NBH, bb = i % NBH;
-                    bool w = mbar_wait(bar_s + buf, (sphase >> buf) & 1u);
-                    sphase ^= 1u << buf;
+                for (int i = 0; i < items; ++i, ++item) {
+                    const uint32_t buf = item % kSB;
+                    const int bt = i / NBH, bb = i % NBH;
+                    bool w = mbar_wait(ready + buf, (item / kSB) & 1);
                     w = __all_sync(0xffffffffu, w);
-                    if (w) {
-                        tc_fence_after();
-                        float *pb = st_best + (bb * kCQ + cq) * kRows + t;
-                        uint32_t *pi = st_bi + (bb * kCQ + cq) * kRows + t;
-                        float best = *pb;
-                        uint32_t bi = *pi;
-                        // This warp's kQC columns of the item, all loads in flight before one wait.
-                        uint32_t rr[kQC / 32][32];
-#pragma unroll
-                        for (int h = 0; h < kQC / 32; ++h)
-                            tmem_ld32_nowait(tmem_base + lane_off + (uint32_t)(buf * kNT + cq * kQC + 32 * h), rr[h]);
-                        tmem_wait_ld();
-                        float cm[kQC / 16];
-#pragma unroll
-                        for (int c = 0; c < kQC / 16; ++c) {
-                            const uint32_t *a = &rr[c / 2][16 * (c % 2)];
-                            float m8[8];
-#pragma unroll
-                            for (int z = 0; z < 8; ++z)
-                                m8[z] = fminf(__uint_as_float(a[2 * z]), __uint_as_float(a[2 * z + 1]));
-#pragma unroll
-                            for (int z = 0; z < 4; ++z) m8[z] = fminf(m8[2 * z], m8[2 * z + 1]);
-                            cm[c] = fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3]));
-                        }
-                        float qmin = cm[0];
-#pragma unroll
-                        for (int c = 1; c < kQC / 16; ++c) qmin = fminf(qmin, cm[c]);
-                        if (qmin < best) {
-                            // The lowest column of this quarter holding the minimum.
-                            best = qmin;
-                            uint32_t j = kQC - 1;
-#pragma unroll
-                            for (int z = kQC - 1; z >= 0; --z)
-                                if (__uint_as_float(rr[z / 32][z % 32]) == qmin) j = (uint32_t)z;
-                            bi = (uint32_t)(bt * kNT + cq * kQC) + j;
-                            *pb = best;
-                            *pi = bi;
-                        }
+                    if (!w) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    float *pb = st_best + (bb * kCQ + cq) * kRows + t;
+                    uint32_t *pi = st_bi + (bb * kCQ + cq) * kRows + t;
+                    float best = *pb;
+                    // This warp's kQC columns of the item, all loads in flight before one wait.
+                    uint32_t rr[kQC / 32][32];
+#pragma unroll
+                    for (int h = 0; h < kQC / 32; ++h)
+                        tmem_ld32_nowait(tmem_base + lane_off + (uint32_t)(buf * kNT + cq * kQC + 32 * h), rr[h]);
+                    tmem_wait_ld();
                     tc_fence_before();
-                    ok = named_sync_and(1, kCons, w && (!lead || iok));
-                    if (!ok) break;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(freeb + buf);      // the buffer's scores are in registers
+                    float cm[kQC / 16];
+#pragma unroll
+                    for (int c = 0; c < kQC / 16; ++c) {
+                        const uint32_t *a = &rr[c / 2][16 * (c % 2)];
+                        float m8[8];
+#pragma unroll
+                        for (int z = 0; z < 8; ++z)
+                            m8[z] = fminf(__uint_as_float(a[2 * z]), __uint_as_float(a[2 * z + 1]));
+#pragma unroll
+                        for (int z = 0; z < 4; ++z) m8[z] = fminf(m8[2 * z], m8[2 * z + 1]);
+                        cm[c] = fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3]));
+                    }
+                    float qmin = cm[0];
+#pragma unroll
+                    for (int c = 1; c < kQC / 16; ++c) qmin = fminf(qmin, cm[c]);
+                    if (qmin < best) {
+                        // The lowest column of this quarter holding the minimum: first the
+                        // 16-column chunk (from the chunk minima), then the column within it.
+                        int c0 = kQC / 16 - 1;
+#pragma unroll
+                        for (int c = kQC / 16 - 1; c >= 0; --c)
+                            if (cm[c] == qmin) c0 = c;
+                        uint32_t j = 15;
+#pragma unroll
+                        for (int c = 0; c < kQC / 16; ++c)
+                            if (c == c0) {
+#pragma unroll
+                                for (int z = 15; z >= 0; --z)
+                                    if (__uint_as_float(rr[c / 2][16 * (c % 2) + z]) == qmin) j = (uint32_t)z;
+                            }
+                        *pb = qmin;
+                        *pi = (uint32_t)(bt * kNT + cq * kQC + c0 * 16) + j;
+                    }
                 }
-                kq += (uint32_t)nbt;
+                ok = named_sync_and(1, kCons, ok);
                 if (!ok) break;
                 // Merge the four column quarters of each block (lowest score, then lowest index),
                 // pack, and free the state for the next pass.
@@ -474,20 +510,16 @@ cudaError_t prepare_kq_tc(fq_ctx *ctx) {
         if (e == cudaSuccess) e = cudaMemcpy(ctx->pi_split, pis.data(), pis.size() * 2, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return e;
     }
-    const bool wide = N % 256 == 0;
-    if (d == 64 && k == 4) return wide ? prep_kq<64, 4, 16, 256>(ctx) : prep_kq<64, 4, 16, 128>(ctx);
-    if (d == 64 && k == 8) return wide ? prep_kq<64, 8, 8, 256>(ctx) : prep_kq<64, 8, 8, 128>(ctx);
+    if (d == 64 && k == 4) return prep_kq<64, 4, 16, 128>(ctx);
+    if (d == 64 && k == 8) return prep_kq<64, 8, 8, 128>(ctx);
     if (d == 128 && k == 4) return prep_kq<128, 4, 8, 128>(ctx);
     return prep_kq<128, 8, 8, 128>(ctx);
 }
 
 cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                 uint32_t *codes, cudaStream_t s) {
-    const bool wide = ctx->N % 256 == 0;
-    if (ctx->d == 64 && ctx->k == 4)
-        return wide ? launch_kq<64, 4, 16, 256>(ctx, x, M, map, nu, codes, s) : launch_kq<64, 4, 16, 128>(ctx, x, M, map, nu, codes, s);
-    if (ctx->d == 64 && ctx->k == 8)
-        return wide ? launch_kq<64, 8, 8, 256>(ctx, x, M, map, nu, codes, s) : launch_kq<64, 8, 8, 128>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64 && ctx->k == 4) return launch_kq<64, 4, 16, 128>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64 && ctx->k == 8) return launch_kq<64, 8, 8, 128>(ctx, x, M, map, nu, codes, s);
     if (ctx->d == 128 && ctx->k == 4) return launch_kq<128, 4, 8, 128>(ctx, x, M, map, nu, codes, s);
     return launch_kq<128, 8, 8, 128>(ctx, x, M, map, nu, codes, s);
 }

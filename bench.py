@@ -60,19 +60,33 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def source_hash() -> str:
-    """Hash of the CUDA sources: ties a committed ncu traffic figure to the kernels it measured."""
+# The source file of each timed kernel; its hash (with the shared headers) ties a committed ncu
+# traffic figure to the code it measured.
+KERNEL_SOURCES = {"encode_k2_tc": "fq_encode_k2.cu", "encode_kq_tc": "fq_encode_kq.cu",
+                  "encode_full_tc": "fq_encode_full_tc.cu", "decode_tc": "fq_decode_tc.cu",
+                  "decode_full_simple": "fq_full.cu"}
+
+
+def source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "random_access_kv_gb300", "csrc")
-    for name in sorted(os.listdir(cdir)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(cdir, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in [KERNEL_SOURCES[kernel], "fq_sm100.cuh", "fq_bits.cuh", "fq_internal.h"]:
+        with open(os.path.join(cdir, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, workload: int):
-    """dram bytes per launch from profiles/<kernel>_w<workload>.md if it was taken on these sources."""
+def kernel_of(w, op: str) -> str:
+    """Name of the kernel that runs `op` ("encode" or "decode") for workload w."""
+    if op == "encode":
+        return "encode_full_tc" if w.k == w.d else ("encode_k2_tc" if w.k == 2 else "encode_kq_tc")
+    return "decode_full_simple" if w.k == w.d else "decode_tc"
+
+
+def committed_traffic(kernel: str, workload: int, rows_per_launch: int):
+    """DRAM bytes per launch from profiles/<kernel>_w<workload>.md, if that capture was taken on the
+    kernel's current sources; a capture of a smaller case is scaled by rows (traffic grows in
+    proportion to the rows a launch processes)."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_w{workload}.md")
     if not os.path.exists(p):
         return None
@@ -82,11 +96,11 @@ def committed_traffic(kernel: str, workload: int):
             if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch")):
                 k, v = line.split(":", 1)
                 vals[k.strip().lstrip("- ")] = v.strip().strip("`")
-    if vals.get("source_hash") != source_hash():
+    if vals.get("source_hash") != source_hash(kernel):
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+        return float(vals["dram_bytes_per_launch"]) * rows_per_launch / float(vals["rows_per_launch"])
+    except (KeyError, ValueError, ZeroDivisionError):
         return None
 
 
@@ -226,11 +240,13 @@ def run_ours(args) -> None:
     if w.op not in ("encode+gather", "encode+decode", "stream+gather"):
         raise SystemExit(f"workload {cfg} ({w.op}) is not timed by bench.py")
     streaming = w.op == "stream+gather"
+    if streaming and args.rows:
+        raise SystemExit("--rows does not apply to the streaming workload")
     gathers = w.op != "encode+decode"            # encode+decode workloads decode every row
     C, Pi = pcb.for_workload(cfg)
     ctx = fq.fq_codebook_load(C, Pi, local)
     R = fq.fq_record_bits(ctx)
-    M, d, nt = w.rows, w.d, w.tensors
+    M, d, nt = (w.rows if not args.rows else min(args.rows, w.rows)), w.d, w.tensors
     # K and V share the codebook and rotation, so they share one code store: rows [t*M, (t+1)*M)
     # hold tensor t. One encode launch covers all tensors, one decode launch all decoded rows.
     MT = nt * M
@@ -247,9 +263,9 @@ def run_ours(args) -> None:
         x_np = np.concatenate([arrival_order(synth.kv_tensor(cfg, t)) for t in range(nt)], axis=1)
         x_np = x_np.reshape(n_steps, nt * n_seq * new, d)
     else:
-        x_np = np.concatenate([synth.kv_tensor(cfg, t) for t in range(nt)])
+        x_np = np.concatenate([synth.kv_tensor(cfg, t, rows=M) for t in range(nt)])
         if gathers:
-            idx_np = np.concatenate([t * M + synth.gather_indices(cfg, t, M, w.gather) for t in range(nt)])
+            idx_np = np.concatenate([t * M + synth.gather_indices(cfg, t, M, min(w.gather, M)) for t in range(nt)])
         else:
             idx_np = np.arange(MT, dtype=np.int64)
     G = int(idx_np.size)
@@ -363,11 +379,13 @@ def run_ours(args) -> None:
     peaks = measured_peaks()
     dec_name = "decode_gather" if gathers else "decode"
     if enc_ms * enc_launches >= gat_ms:
-        dom, dom_bytes, dom_ms = "encode", enc_b * enc_rows, enc_ms
-        kname = "fq_encode_append" if streaming else "fq_encode"
+        dom, dom_bytes, dom_ms, dom_rows = "encode", enc_b * enc_rows, enc_ms, enc_rows
+        kname = kernel_of(w, "encode")
     else:
-        dom, dom_bytes, dom_ms, kname = dec_name, gat_b * G, gat_ms, "fq_" + dec_name
-    roofline = {"kernel": dom, "traffic": committed_traffic(kname, cfg), "peak_source": peaks["source"],
+        dom, dom_bytes, dom_ms, dom_rows = dec_name, gat_b * G, gat_ms, G
+        kname = kernel_of(w, "decode")
+    roofline = {"kernel": dom, "cuda_kernel": kname, "traffic": committed_traffic(kname, cfg, dom_rows),
+                "peak_source": peaks["source"],
                 "algorithmic_bytes_per_launch": int(dom_bytes), "launch_ms": round(dom_ms, 5),
                 "encode_launch_ms": round(enc_ms, 5), "encode_rows_per_launch": enc_rows,
                 f"{dec_name}_launch_ms": round(gat_ms, 5), f"{dec_name}_rows_per_launch": G,
@@ -392,7 +410,7 @@ def run_ours(args) -> None:
                "sample": r["sample"], "seconds": round(r["seconds"], 2)}
 
     if rank == 0:
-        conf = {"workload": w.name, "rows_per_tensor": M, "tensors": nt, "d": d, "k": w.k, "N": w.N,
+        conf = {"workload": w.name + (f" (first {M} rows per tensor)" if M != w.rows else ""), "rows_per_tensor": M, "tensors": nt, "d": d, "k": w.k, "N": w.N,
                 "bits_per_coordinate": w.B / w.k, "record_bits": R,
                 ("gathered_rows" if gathers else "decoded_rows"): G,
                 "layout": "K and V in one code store; one encode and one decode launch per step"
@@ -430,6 +448,9 @@ def main():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="rows per tensor (a prefix of the workload; a small case for profiling). "
+                         "Not for the streaming workload.")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

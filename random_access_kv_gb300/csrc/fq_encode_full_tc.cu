@@ -194,12 +194,7 @@ encode_full_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
                             sc[4 * q + 2] = fmaf(__uint_as_float(a[4 * q + 2]), rs, hv.z);
                             sc[4 * q + 3] = fmaf(__uint_as_float(a[4 * q + 3]), rs, hv.w);
                         }
-                        float m8[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) m8[q] = fminf(sc[2 * q], sc[2 * q + 1]);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) m8[q] = fminf(m8[2 * q], m8[2 * q + 1]);
-                        const float cmin = fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3]));
+                        const float cmin = min16(sc);
                         if (cmin < best) {
                             best = cmin;
                             uint32_t j = 15;

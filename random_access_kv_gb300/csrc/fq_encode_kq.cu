@@ -344,14 +344,10 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     float cm[kQC / 16];
 #pragma unroll
                     for (int c = 0; c < kQC / 16; ++c) {
-                        const uint32_t *a = &rr[c / 2][16 * (c % 2)];
-                        float m8[8];
+                        float v16[16];
 #pragma unroll
-                        for (int z = 0; z < 8; ++z)
-                            m8[z] = fminf(__uint_as_float(a[2 * z]), __uint_as_float(a[2 * z + 1]));
-#pragma unroll
-                        for (int z = 0; z < 4; ++z) m8[z] = fminf(m8[2 * z], m8[2 * z + 1]);
-                        cm[c] = fminf(fminf(m8[0], m8[1]), fminf(m8[2], m8[3]));
+                        for (int z = 0; z < 16; ++z) v16[z] = __uint_as_float(rr[c / 2][16 * (c % 2) + z]);
+                        cm[c] = min16(v16);
                     }
                     float qmin = cm[0];
 #pragma unroll

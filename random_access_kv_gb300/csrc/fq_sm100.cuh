@@ -218,6 +218,20 @@ __device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t count, bool
     return out != 0;
 }
 
+// Three-input minimum (one instruction on sm_100-family parts).
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Minimum of 16 values in 8 instructions.
+__device__ __forceinline__ float min16(const float (&v)[16]) {
+    const float a = fmin3(v[0], v[1], v[2]), b = fmin3(v[3], v[4], v[5]), c = fmin3(v[6], v[7], v[8]);
+    const float d = fmin3(v[9], v[10], v[11]), e = fmin3(v[12], v[13], v[14]);
+    return fminf(fmin3(a, b, c), fmin3(d, e, v[15]));
+}
+
 // Split of a float into fp16 hi + lo halves (hi = rn(v), lo = rn(v - hi)), packed for two values.
 __device__ __forceinline__ void split_half2(float a, float b, uint32_t &hi, uint32_t &lo) {
     const __half2 h = __floats2half2_rn(a, b);

@@ -93,7 +93,8 @@ def committed_traffic(kernel: str, workload: int, rows_per_launch: int):
     vals = {}
     with open(p) as f:
         for line in f:
-            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch")):
+            if ":" in line and line.strip().lstrip("- ").startswith(
+                    ("source_hash", "dram_bytes_per_launch", "rows_per_launch")):
                 k, v = line.split(":", 1)
                 vals[k.strip().lstrip("- ")] = v.strip().strip("`")
     if vals.get("source_hash") != source_hash(kernel):

@@ -127,6 +127,17 @@ def unpack(words, M: int, nb: int, B: int) -> np.ndarray:
     return np.sum(b << np.arange(B), axis=2)
 
 
+def record_range(words, m0: int, count: int, nb: int, B: int) -> np.ndarray:
+    """Indices [count, nb] of the consecutive records m0 .. m0 + count - 1, read from their fixed
+    addresses (record m starts at bit m R) [FibQuant §1, §2.3]."""
+    R = nb * B
+    lo, hi = m0 * R, (m0 + count) * R
+    w = np.asarray(words, dtype=np.uint32)[lo // 32:(hi + 31) // 32].astype(np.uint64)
+    bits = ((w[:, None] >> np.arange(32, dtype=np.uint64)) & 1).reshape(-1)
+    b = bits[lo % 32:lo % 32 + count * R].reshape(count, nb, B).astype(np.int64)
+    return np.sum(b << np.arange(B), axis=2)
+
+
 def record_indices(words, m: int, nb: int, B: int) -> np.ndarray:
     """Indices of the single record m, read bit by bit from its fixed address m R: the random
     access that the fixed-rate layout allows [FibQuant §1]."""

@@ -13,7 +13,8 @@ distributions described per workload below.
 
 Random streams: ``rng(cfg, stream, *sub)`` is ``numpy.random.default_rng([cfg, stream, *sub])``.
 Stream 0 = K data, 1 = V data, 2 = the Gaussian matrix behind the rotation, 3 = codebook
-building (Lloyd training draws, restart rotations, Kronecker offset), 4 = gather indices.
+building (Lloyd training draws, restart rotations, Kronecker offset), 4 = gather indices,
+5 = attention queries, 6 = random code stores.
 """
 from __future__ import annotations
 
@@ -23,6 +24,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 STREAM_K, STREAM_V, STREAM_ROT, STREAM_CODEBOOK, STREAM_GATHER = 0, 1, 2, 3, 4
+STREAM_QUERY, STREAM_STORE = 5, 6
 
 
 def rng(cfg: int, stream: int, *sub: int) -> np.random.Generator:
@@ -182,3 +184,19 @@ def gather_indices(cfg: int, which: int, M: int, n: int, replace: bool = True) -
 def token_positions(cfg: int, T: int, n: int) -> np.ndarray:
     """n distinct token positions in [0, T), random order (shared by all layers and heads)."""
     return rng(cfg, STREAM_GATHER, 9).permutation(T)[:n].astype(np.int64)
+
+
+def query_rows(cfg: int, n: int, d: int, sub: int = 0) -> np.ndarray:
+    """Attention queries: n fp16 rows [n, d] of N(0, 1) entries (stream 5)."""
+    return rng(cfg, STREAM_QUERY, sub).standard_normal((n, d)).astype(np.float16)
+
+
+def random_store(cfg: int, M: int, n_words: int, sub: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """A code store of M rows with uniformly random bits and log-normal norms (stream 6):
+    (nu float32 [M], words uint32 [n_words]). With N a power of two every bit pattern is a valid
+    record, so this exercises all codewords without running an encoder. Norms are
+    exp(N(log 8, 0.5^2)), about the norm of a 64-dimensional row of unit-variance entries."""
+    r = rng(cfg, STREAM_STORE, sub)
+    nu = np.exp(r.normal(np.log(8.0), 0.5, size=M)).astype(np.float32)
+    words = r.integers(0, 1 << 32, size=n_words, dtype=np.uint64).astype(np.uint32)
+    return nu, words

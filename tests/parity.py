@@ -10,6 +10,16 @@ Tolerances, from the codec's contract and the arithmetic of the fp32/fp16 device
   decode   : device decode of the device's codes within 1e-4 nu (max-abs) of the oracle's fp64
              decode of the same codes, before the fp16 rounding; after it, plus half an fp16 ulp
              of the oracle's value.
+  attention: fused attention (fp32 throughout) within, per output element,
+               u [ 2 lam (d + sqrt d + 2) A V_inf + lam (2 sqrt(T + 64) + sqrt d + 8) sqrt d V_2 ]
+             of the oracle's fp64 attention over the decoded keys and values; u = 2^-24,
+             A = scale |q| max_t |k_hat_t| bounds the scores, V_inf / V_2 = max_t of |v_hat_t| in
+             the max / Euclidean norm. First term: the score error (rotation of q, d-term dot
+             products, the two scalings) moves the softmax output by at most twice the score error
+             times V_inf. Second term: the value sums of up to T + 64 terms, the normaliser and
+             the d-term inverse rotation. Each sum of n rounded terms is bounded by
+             lam sqrt(n) u (Higham and Mary's probabilistic rounding-error bound, lam = 8: it
+             fails with probability below 2 exp(-lam^2 / 2) ~ 3e-14 per sum).
 """
 from __future__ import annotations
 
@@ -76,3 +86,32 @@ def check_decode(out_gpu, nu, idx, C, Pi, fp16_output: bool):
     assert not bad.any(), f"decode error {err[bad][:5]} > tol {tol[bad][:5]} at {np.argwhere(bad)[:3]}"
     nz = np.asarray(nu) > 0
     return float((err[nz] / np.asarray(nu)[nz, None]).max()) if nz.any() else 0.0
+
+
+ATT_LAMBDA = 8.0
+
+
+def attention_tolerance(q, K_hat, V_hat, scale) -> np.ndarray:
+    """Per-query max-abs tolerance of the fused attention output (see the module docstring)."""
+    u = 2.0 ** -24
+    q = np.atleast_2d(np.asarray(q, dtype=np.float64))
+    T, d = K_hat.shape
+    A = abs(scale) * np.linalg.norm(q, axis=1) * np.linalg.norm(K_hat, axis=1).max()
+    v_inf = np.abs(V_hat).max()
+    v_2 = np.linalg.norm(V_hat, axis=1).max()
+    lam = ATT_LAMBDA
+    return u * (2 * lam * (d + np.sqrt(d) + 2) * A * v_inf
+                + lam * (2 * np.sqrt(T + 64) + np.sqrt(d) + 8) * np.sqrt(d) * v_2)
+
+
+def check_attention(out_gpu, q, nu_k, idx_k, nu_v, idx_v, C, Pi, scale):
+    """Fused attention of one group's queries vs the oracle. Returns the max of error / tolerance."""
+    from oracle import attention as oat
+    ref = oat.attention_decode(q, nu_k, idx_k, nu_v, idx_v, C, Pi, scale)
+    K_hat = ofq.decode(nu_k, idx_k, C, Pi)
+    V_hat = ofq.decode(nu_v, idx_v, C, Pi)
+    tol = attention_tolerance(q, K_hat, V_hat, scale)[:, None]
+    err = np.abs(np.asarray(out_gpu, dtype=np.float64) - ref)
+    bad = err > tol
+    assert not bad.any(), f"attention error {err[bad][:5]} > tol {np.broadcast_to(tol, err.shape)[bad][:5]}"
+    return float((err / tol).max())

@@ -11,10 +11,16 @@ live in one code store, so each step is one encode launch and one gather launch.
 the timed region starts; L2 is flushed (a 256 MB write) before every timed step, outside the
 step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it.
 
+`--attend` times fused decode-into-attention instead: the workload's K and V are encoded into one
+store (untimed), then each step is one launch in which one fp16 query per (layer, head) group
+attends over all T cached tokens of its group, decoding keys and values inside the kernel. The
+metric is then cached K/V vectors read per second, and the line carries the attention-output
+cosine against the same attention over the uncompressed fp16 K/V.
+
 `--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
 sample of the same workload instead.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2] [--attend]
 """
 from __future__ import annotations
 
@@ -36,6 +42,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "KV vectors/s encoded and decoded (fp16 GB/s) per bitrate; % of HBM/TC roofline"
+ATTEND_METRIC = "cached KV vectors/s attended (fused decode-into-attention, one query per head)"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -64,7 +71,7 @@ def measured_peaks() -> dict:
 # traffic figure to the code it measured.
 KERNEL_SOURCES = {"encode_k2_tc": "fq_encode_k2.cu", "encode_kq_tc": "fq_encode_kq.cu",
                   "encode_full_tc": "fq_encode_full_tc.cu", "decode_tc": "fq_decode_tc.cu",
-                  "decode_full_simple": "fq_full.cu"}
+                  "decode_full_simple": "fq_full.cu", "attend": "fq_attend.cu"}
 
 
 def source_hash(kernel: str) -> str:
@@ -196,16 +203,48 @@ def time_oracle(cfg: int, steps: int) -> dict:
                       f"of workload {cfg}, {steps} steps, numpy fp64"}
 
 
+def attend_groups(w) -> tuple[int, int]:
+    """(groups, tokens per group) of a two-tensor workload: a group is one (layer, head[, batch])
+    sequence of T = shape[-2] tokens, contiguous in the tensor's rows."""
+    T = int(w.shape[-2])
+    return w.rows // T, T
+
+
+def time_oracle_attend(cfg: int, steps: int) -> dict:
+    from oracle import attention as oat
+    from oracle import fibquant as ofq
+    from oracle import workloads as ow
+    w = synth.WORKLOADS[cfg]
+    C, Pi = ow.codebook(cfg), ow.rotation(cfg)
+    _, T = attend_groups(w)
+    groups = 2
+    x = [synth.kv_tensor(cfg, t, rows=groups * T) for t in range(2)]
+    q = synth.query_rows(cfg, groups, w.d)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        enc = [ofq.encode(xt, C, Pi) for xt in x]
+        for g in range(groups):
+            sl = slice(g * T, (g + 1) * T)
+            oat.attention_decode(q[g], enc[0][0][sl], enc[0][1][sl], enc[1][0][sl], enc[1][1][sl], C, Pi,
+                                 1.0 / np.sqrt(w.d))
+    dt = time.perf_counter() - t0
+    vecs = steps * groups * 2 * T
+    return {"value": vecs / dt, "seconds": dt, "vectors": vecs,
+            "sample": f"{groups} groups x {T} tokens of workload {cfg} (K and V encoded, then decoded and "
+                      f"attended by one query each), {steps} steps, numpy fp64"}
+
+
 def run_reference(args) -> None:
     rank, world, _ = dist_env()
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
-    time_oracle(args.workload, max(1, args.warmup))
-    r = time_oracle(args.workload, args.steps)
+    timer = time_oracle_attend if args.attend else time_oracle
+    timer(args.workload, max(1, args.warmup))
+    r = timer(args.workload, args.steps)
     cores = host_cores()
     line = {
-        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "vectors/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": ATTEND_METRIC if args.attend else METRIC, "value": r["value"], "unit": "vectors/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r["seconds"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": r["sample"]},
@@ -440,6 +479,179 @@ def run_ours(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+def run_attend(args) -> None:
+    import torch
+    import random_access_kv_gb300 as fq
+    from random_access_kv_gb300 import build as fbuild
+    from random_access_kv_gb300 import codebook as pcb
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    cfg = args.workload
+    w = synth.WORKLOADS[cfg]
+    if w.tensors != 2:
+        raise SystemExit(f"workload {cfg} has no separate keys and values")
+    C, Pi = pcb.for_workload(cfg)
+    ctx = fq.fq_codebook_load(C, Pi, local)
+    R = fq.fq_record_bits(ctx)
+    groups, T = attend_groups(w)
+    M, d = w.rows, w.d
+    scale = 1.0 / float(np.sqrt(d))
+    # The cache: K rows [0, M), V rows [M, 2M) of one store, encoded once (untimed).
+    nu, codes = fq.alloc_store(ctx, 2 * M, dev)
+    for t in range(2):
+        x = torch.from_numpy(synth.kv_tensor(cfg, t)).to(dev)
+        fq.fq_encode(ctx, x, M, nu, codes, t * M)
+        del x
+    torch.cuda.synchronize(dev)
+    q_host = torch.from_numpy(synth.query_rows(cfg, groups, d)).pin_memory()
+    q = q_host.to(dev)
+    out = torch.empty((groups, d), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step():
+        fq.fq_attend(ctx, nu, codes, 2 * M, q, groups, 1, T, 0, M, T, scale, out, sp)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fq.fq_status(ctx, sp) != 0:
+        raise SystemExit("device flags set during warm-up")
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = sum(ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    vec_per_step = 2 * groups * T
+    value = world * vec_per_step * args.steps / (total_ms / 1e3)
+
+    # End to end: the cache stays resident (it is the KV cache); each step copies its queries in
+    # from pinned host memory and the attention outputs back.
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    e2e_ms = []
+    for i in range(args.steps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q.copy_(q_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = sum(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * vec_per_step * args.steps / (e2e_total / 1e3)
+
+    # Fidelity: cosine with exact attention (fp64 on the device) over the uncompressed fp16 K and V,
+    # and, as a full-size consistency check of the fused kernel, over the same cache decoded by
+    # the library's separate decoder.
+    o_fused = out.double()
+    cos, cos_dec = [], []
+    k_all, v_all = synth.kv_tensor(cfg, 0), synth.kv_tensor(cfg, 1)
+
+    def attention(Kx, Vx, qx):
+        p = torch.softmax(scale * torch.einsum("gtd,gd->gt", Kx, qx), dim=1)
+        return torch.einsum("gt,gtd->gd", p, Vx)
+
+    for g0 in range(0, groups, 64):
+        g1 = min(groups, g0 + 64)
+        n = (g1 - g0) * T
+        Kx = torch.from_numpy(k_all[g0 * T:g1 * T]).to(dev).double().view(g1 - g0, T, d)
+        Vx = torch.from_numpy(v_all[g0 * T:g1 * T]).to(dev).double().view(g1 - g0, T, d)
+        cos.append(torch.nn.functional.cosine_similarity(attention(Kx, Vx, q[g0:g1].double()),
+                                                         o_fused[g0:g1], dim=1).cpu())
+        del Kx, Vx
+        rows = torch.arange(g0 * T, g1 * T, device=dev)
+        dec = torch.empty((2 * n, d), dtype=torch.float32, device=dev)
+        fq.fq_decode_gather_f32(ctx, nu, codes, 2 * M, torch.cat([rows, rows + M]), 2 * n, dec, sp)
+        dec = dec.double().view(2, g1 - g0, T, d)
+        cos_dec.append(torch.nn.functional.cosine_similarity(attention(dec[0], dec[1], q[g0:g1].double()),
+                                                             o_fused[g0:g1], dim=1).cpu())
+        del dec
+    del k_all, v_all
+    cos = torch.cat(cos).numpy()
+    cos_dec = torch.cat(cos_dec).numpy()
+    flags = fq.fq_status(ctx, sp)
+
+    launch_ms = statistics.mean(ms)
+    alg_bytes = groups * T * 2 * (R / 8 + 4) + groups * d * (2 + 4)
+    peaks = measured_peaks()
+    achieved = alg_bytes / (launch_ms / 1e3) / 1e9
+    roofline = {"kernel": "attend", "cuda_kernel": "attend", "traffic": committed_traffic("attend", cfg, groups * T),
+                "peak_source": peaks["source"], "algorithmic_bytes_per_launch": int(alg_bytes),
+                "launch_ms": round(launch_ms, 5), "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_oracle_attend(cfg, args.cpu_steps)
+        cpu = {"value": r["value"], "unit": "vectors/s", "cores": host_cores(), "kind": "oracle",
+               "sample": r["sample"], "seconds": round(r["seconds"], 2)}
+    if rank == 0:
+        line = {
+            "metric": ATTEND_METRIC, "value": value, "unit": "vectors/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name + " -- fused attention", "groups": groups, "tokens_per_group": T,
+                       "queries_per_group": 1, "d": d, "k": w.k, "N": w.N, "record_bits": R,
+                       "layout": "K rows [0, M), V rows [M, 2M) of one code store; one launch per step",
+                       "l2": "flushed before every timed step (256 MB write, outside the step events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "fidelity": {"attention_cosine_mean": float(cos.mean()), "attention_cosine_min": float(cos.min()),
+                         "against": "softmax attention over the uncompressed fp16 K/V, fp64",
+                         "queries": "N(0, 1) fp16, independent of the keys",
+                         "unfused_cosine_min": float(cos_dec.min()),
+                         "unfused": "softmax attention, fp64, over the same cache decoded by fq_decode_gather_f32"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "vectors/s", "h2d_bytes_per_step": int(q_host.numel() * 2),
+                    "d2h_bytes_per_step": int(out_host.numel() * 4)},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "device_flags": flags,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -448,6 +660,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--attend", action="store_true", help="time fused decode-into-attention")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per tensor (a prefix of the workload; a small case for profiling). "
@@ -457,6 +670,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.attend:
+        run_attend(args)
     else:
         run_ours(args)
 

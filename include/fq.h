@@ -127,6 +127,28 @@ int fq_decode_gather(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_
 int fq_decode_gather_f32(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
                          const int64_t *idx, int64_t n, float *out, void *stream);
 
+/*
+ * fq_attend - single-query softmax attention over compressed keys and values, decoded inside the
+ * kernel [FibQuant §5: the fixed-address interface lets decompression fuse into attention; §2.3
+ * decoder]. For query r (group g = r / q_per_group):
+ *   o_r = sum_t p_t x_hat(v_row0 + g stride + t) / sum_t p_t,
+ *   p_t = exp(s_t - max_t s_t),  s_t = scale * q_r . x_hat(k_row0 + g stride + t),  t < T,
+ * where x_hat(m) is the decode of store row m (as fq_decode, before fp16 rounding).
+ *   nu, codes   : the store of M rows (keys and values of all groups in one store);
+ *   q           : device fp16 [n_queries x d], row-major;
+ *   n_queries   : a multiple of q_per_group (queries sharing one cached group, >= 1);
+ *   T           : cached tokens per group, >= 1;
+ *   k_row0, v_row0, stride : row of key/value token t of group g is row0 + g * stride + t; every
+ *                 such row must lie in [0, M) (else FQ_EINVAL);
+ *   scale       : finite score scale (commonly 1/sqrt(d));
+ *   out         : device float32 [n_queries x d].
+ * Non-finite norms in the store give non-finite outputs. Returns FQ_EINVAL when the codebook and
+ * record staging of this context do not fit one CTA's shared memory.
+ */
+int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, const void *q,
+              int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,
+              int64_t stride, float scale, float *out, void *stream);
+
 /* Number of uint32 words of a store of M records: ceil(M R / 32). Returns -1 on bad arguments. */
 int64_t fq_code_words(const fq_ctx *ctx, int64_t M);
 

@@ -40,6 +40,8 @@ _SIGNATURES = {
     "fq_decode": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p]),
     "fq_decode_gather": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
     "fq_decode_gather_f32": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fq_attend": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _i64, _i64, _i64, _i64, _i64,
+                         ctypes.c_float, _c_void_p, _c_void_p]),
     "fq_code_words": (_i64, [_c_void_p, _i64]),
     "fq_record_bits": (_int, [_c_void_p]),
     "fq_shape": (_int, [_c_void_p, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
@@ -164,6 +166,13 @@ def fq_decode_gather(ctx: Context, nu, codes, M: int, idx, n: int, out, stream=N
 def fq_decode_gather_f32(ctx: Context, nu, codes, M: int, idx, n: int, out, stream=None) -> None:
     _check("fq_decode_gather_f32", lib().fq_decode_gather_f32(ctx, _ptr(nu), _ptr(codes), int(M), _ptr(idx),
                                                               int(n), _ptr(out), _stream(stream)))
+
+
+def fq_attend(ctx: Context, nu, codes, M: int, q, n_queries: int, q_per_group: int, T: int, k_row0: int,
+              v_row0: int, stride: int, scale: float, out, stream=None) -> None:
+    _check("fq_attend", lib().fq_attend(ctx, _ptr(nu), _ptr(codes), int(M), _ptr(q), int(n_queries),
+                                        int(q_per_group), int(T), int(k_row0), int(v_row0), int(stride),
+                                        float(scale), _ptr(out), _stream(stream)))
 
 
 def fq_code_words(ctx: Context, M: int) -> int:

@@ -111,6 +111,7 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     c->nb = d / k;
     c->R = c->nb * B;
     c->num_sms = prop.multiProcessorCount;
+    c->smem_optin = (int)prop.sharedMemPerBlockOptin;
 
     std::vector<float> C(C_host, C_host + (size_t)N * k);
     std::vector<float> P(Pi_host, Pi_host + (size_t)d * d);
@@ -146,6 +147,7 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
     if (e == cudaSuccess && is_full(c) && fq::full_tc_supported(c)) e = fq::prepare_full_tc(c);
     if (e == cudaSuccess && !is_full(c) && !c->grid2 && fq::kq_tc_supported(c)) e = fq::prepare_kq_tc(c);
+    if (e == cudaSuccess) e = fq::prepare_attend(c);
     if (e != cudaSuccess) {
         const int rc = (e == cudaErrorMemoryAllocation) ? FQ_ENOMEM : FQ_ECUDA;
         free_ctx(c);
@@ -247,6 +249,30 @@ int fq_decode_gather_f32(fq_ctx *ctx, const float *nu, const uint32_t *codes, in
                          const int64_t *idx, int64_t n, float *out, void *stream) {
     if (n > 0 && !idx) return FQ_EINVAL;
     return decode_common(ctx, nu, codes, M, idx, n, out, true, stream);
+}
+
+int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, const void *q,
+              int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,
+              int64_t stride, float scale, float *out, void *stream) {
+    if (!ctx || M < 0 || n_queries < 0 || q_per_group < 1 || T < 1) return FQ_EINVAL;
+    if (k_row0 < 0 || v_row0 < 0 || stride < 0 || !isfinite(scale)) return FQ_EINVAL;
+    if (n_queries % q_per_group || n_queries > INT32_MAX / 8) return FQ_EINVAL;
+    if (n_queries == 0) return FQ_OK;
+    if (!nu || !codes || !q || !out) return FQ_EINVAL;
+    if (fq_code_words(ctx, M) < 0) return FQ_EINVAL;
+    // Every cached row of every group lies in [0, M).
+    const int64_t groups = n_queries / q_per_group;
+    for (int64_t r0 : {k_row0, v_row0}) {
+        if (T > M || r0 > M - T) return FQ_EINVAL;
+        if (groups > 1 && stride > (M - T - r0) / (groups - 1)) return FQ_EINVAL;
+    }
+    if (!aligned(nu, 4) || !aligned(codes, 4) || !aligned(q, 2) || !aligned(out, 4)) return FQ_EALIGN;
+    if (!ctx->attend_nwarps) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    cudaError_t e = fq::launch_attend(ctx, nu, codes, (const __half *)q, n_queries, q_per_group, T, k_row0,
+                                      v_row0, stride, scale, out, (cudaStream_t)stream);
+    return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
 }
 
 int fq_status(fq_ctx *ctx, void *stream, uint32_t *flags) {

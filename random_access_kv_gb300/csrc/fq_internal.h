@@ -32,6 +32,10 @@ struct fq_ctx {
     // k = 4, 8 tensor-core encoder table
     uint8_t *cb_ops;             // codebook rows as MMA B operands (see fq_encode_kq.cu)
     int kq_max_ctas;
+    // fused attention launch shape (attend_nwarps == 0: the configuration does not fit)
+    int smem_optin;              // dynamic shared memory a CTA may opt in to
+    int attend_lut, attend_nwarps, attend_max_split, attend_per_sm;
+    size_t attend_smem;
 };
 
 namespace fq {
@@ -80,6 +84,11 @@ bool kq_tc_supported(const fq_ctx *ctx);
 cudaError_t prepare_kq_tc(fq_ctx *ctx);
 cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                 uint32_t *codes, cudaStream_t s);
+cudaError_t prepare_attend(fq_ctx *ctx);
+cudaError_t launch_attend(const fq_ctx *ctx, const float *nu, const uint32_t *codes, const __half *q,
+                          int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,
+                          int64_t stride, float scale, float *out, cudaStream_t s);
+int attend_split(const fq_ctx *ctx, int64_t n_queries, int64_t T);
 // One-time kernel attribute set-up (dynamic shared memory limits); called by fq_codebook_load.
 cudaError_t prepare_encode_blocks(const fq_ctx *ctx);
 cudaError_t prepare_decode_blocks(const fq_ctx *ctx);

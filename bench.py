@@ -504,12 +504,14 @@ def run_attend(args) -> None:
     ctx = fq.fq_codebook_load(C, Pi, local)
     R = fq.fq_record_bits(ctx)
     groups, T = attend_groups(w)
-    M, d = w.rows, w.d
+    if args.groups:
+        groups = min(groups, args.groups)
+    M, d = groups * T, w.d
     scale = 1.0 / float(np.sqrt(d))
     # The cache: K rows [0, M), V rows [M, 2M) of one store, encoded once (untimed).
     nu, codes = fq.alloc_store(ctx, 2 * M, dev)
     for t in range(2):
-        x = torch.from_numpy(synth.kv_tensor(cfg, t)).to(dev)
+        x = torch.from_numpy(synth.kv_tensor(cfg, t, rows=M)).to(dev)
         fq.fq_encode(ctx, x, M, nu, codes, t * M)
         del x
     torch.cuda.synchronize(dev)
@@ -583,7 +585,7 @@ def run_attend(args) -> None:
     # the library's separate decoder.
     o_fused = out.double()
     cos, cos_dec = [], []
-    k_all, v_all = synth.kv_tensor(cfg, 0), synth.kv_tensor(cfg, 1)
+    k_all, v_all = synth.kv_tensor(cfg, 0, rows=M), synth.kv_tensor(cfg, 1, rows=M)
 
     def attention(Kx, Vx, qx):
         p = torch.softmax(scale * torch.einsum("gtd,gd->gt", Kx, qx), dim=1)
@@ -628,7 +630,8 @@ def run_attend(args) -> None:
             "metric": ATTEND_METRIC, "value": value, "unit": "vectors/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name + " -- fused attention", "groups": groups, "tokens_per_group": T,
+            "config": {"workload": w.name + " -- fused attention"
+                       + (f" (first {groups} groups)" if groups * T != w.rows else ""), "groups": groups, "tokens_per_group": T,
                        "queries_per_group": 1, "d": d, "k": w.k, "N": w.N, "record_bits": R,
                        "layout": "K rows [0, M), V rows [M, 2M) of one code store; one launch per step",
                        "l2": "flushed before every timed step (256 MB write, outside the step events)",
@@ -661,6 +664,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--attend", action="store_true", help="time fused decode-into-attention")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="with --attend: the first G (layer, head) groups only (a small case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per tensor (a prefix of the workload; a small case for profiling). "

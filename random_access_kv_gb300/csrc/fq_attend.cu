@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "fq_internal.h"
 #include "fq_sm100.cuh"
@@ -89,23 +90,36 @@ __device__ __forceinline__ float transpose_sum(float (&v)[NP], int lane) {
     return v[0];
 }
 
-// B-bit field at bit p of a staged word array (the field may straddle two words).
+// B-bit field at bit p of a staged word array. ONE: the field lies within one word (B divides
+// 32 and the tile's fields start on multiples of B); otherwise it may straddle two words.
+template <bool ONE>
 __device__ __forceinline__ uint32_t field(const uint32_t *w, int p, uint32_t mask) {
-    return __funnelshift_r(w[p >> 5], w[(p >> 5) + 1], p & 31) & mask;
+    if constexpr (ONE)
+        return (w[p >> 5] >> (p & 31)) & mask;
+    else
+        return __funnelshift_r(w[p >> 5], w[(p >> 5) + 1], p & 31) & mask;
+}
+
+// Codebook rows in shared memory. For k = 8 a row is two 16-byte halves; storing them swapped in
+// rows with bit 2 of n set spreads the halves that the lanes of a quarter-warp read over all eight
+// 4-bank groups (unswizzled, every first half falls in an even group).
+template <int K>
+__device__ __forceinline__ int codeword_slot(int n, int half) {
+    return K == 8 ? n * 8 + 4 * (half ^ ((n >> 2) & 1)) : n * K + 4 * half;
 }
 
 template <int K>
-__device__ __forceinline__ void load_codeword(const float *c, float (&v)[K]) {
+__device__ __forceinline__ void load_codeword(const float *Cs, uint32_t n, float (&v)[K]) {
     if constexpr (K == 1) {
-        v[0] = c[0];
+        v[0] = Cs[n];
     } else if constexpr (K == 2) {
-        const float2 a = *reinterpret_cast<const float2 *>(c);
+        const float2 a = *reinterpret_cast<const float2 *>(Cs + 2 * n);
         v[0] = a.x, v[1] = a.y;
     } else {
 #pragma unroll
-        for (int j = 0; j < K; j += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(c + j);
-            v[j] = a.x, v[j + 1] = a.y, v[j + 2] = a.z, v[j + 3] = a.w;
+        for (int h = 0; h < K / 4; ++h) {
+            const float4 a = *reinterpret_cast<const float4 *>(Cs + codeword_slot<K>(n, h));
+            v[4 * h] = a.x, v[4 * h + 1] = a.y, v[4 * h + 2] = a.z, v[4 * h + 3] = a.w;
         }
     }
 }
@@ -159,49 +173,6 @@ attend_kernel(const AttendArgs a) {
     const uint32_t mask = (uint32_t)N - 1u;
     const int64_t T = a.T;
 
-    for (int i = threadIdx.x; i < D; i += blockDim.x) qs[i] = __half2float(a.q[query * D + i]);
-    if constexpr (!FULL)
-        for (int i = threadIdx.x; i < N * K; i += blockDim.x) Cs[i] = __ldg(a.C + i);
-    __syncthreads();
-    if constexpr (!FULL) {
-        // q~ = Pi q: warp w takes rows w, w + nwarps, ... with the lanes along the row.
-        for (int i = warp; i < D; i += nwarps) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = lane; j < D; j += 32) acc = fmaf(__ldg(a.Pi + (int64_t)i * D + j), qs[j], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) qt[i] = acc;
-        }
-        __syncthreads();
-        if constexpr (LUT) {
-            for (int e = threadIdx.x; e < N * LP; e += blockDim.x) {
-                const int n = e / LP, slot = e % LP;
-                const int b = (NB >= 32) ? slot : slot % NB;
-                float c[K];
-                load_codeword<K>(Cs + n * K, c);
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 0; j < K; ++j) acc = fmaf(qt[b * K + j], c[j], acc);
-                Ls[e] = acc;
-            }
-            __syncthreads();
-        }
-    }
-
-    // The lane's query coordinates: k <= 8 without a table: its blocks of q~; k = d: q itself.
-    float qreg[FULL ? D / 32 : (LUT ? 1 : K * SPT)];
-    if constexpr (FULL) {
-#pragma unroll
-        for (int s = 0; s < D / 32; ++s) qreg[s] = qs[s * 32 + lane];
-    } else if constexpr (!LUT) {
-#pragma unroll
-        for (int s = 0; s < SPT; ++s) {
-            const int b = (NB >= 32) ? s * 32 + lane : lane % NB;
-#pragma unroll
-            for (int j = 0; j < K; ++j) qreg[s * K + j] = qt[b * K + j];
-        }
-    }
-
     // This CTA's tiles, dealt to its warps round-robin.
     const int64_t n_tiles = (T + 31) / 32;
     const int64_t tile_lo = n_tiles * rank / a.split, tile_hi = n_tiles * (rank + 1) / a.split;
@@ -225,13 +196,71 @@ attend_kernel(const AttendArgs a) {
         cp_async_commit();
     };
 
+    // The first tile's records are requested before the tables are built, to overlap their latency.
+    int64_t tile = tile_lo + warp;
+    if (tile < tile_hi) issue(tile, 0);
+
+    for (int i = threadIdx.x; i < D; i += blockDim.x) qs[i] = __half2float(a.q[query * D + i]);
+    if constexpr (!FULL)
+        for (int i = threadIdx.x; i < N * K; i += blockDim.x)
+            Cs[K == 8 ? codeword_slot<K>(i / 8, (i / 4) & 1) + (i & 3) : i] = __ldg(a.C + i);
+    __syncthreads();
+    if constexpr (!FULL) {
+        // q~ = Pi q: tpr consecutive threads per row (whole warps), each a contiguous chunk of it,
+        // with all of a thread's loads in flight together.
+        int tpr = 1;
+        while (tpr < 8 && 2 * tpr * D <= (int)blockDim.x) tpr *= 2;
+        if ((int)threadIdx.x < tpr * D) {
+            const int i = threadIdx.x / tpr, part = threadIdx.x % tpr, chunk = D / tpr;
+            const float4 *prow = reinterpret_cast<const float4 *>(a.Pi + (int64_t)i * D + part * chunk);
+            const float *qq = qs + part * chunk;
+            float acc = 0.f;
+#pragma unroll 8
+            for (int j = 0; j < chunk / 4; ++j) {
+                const float4 p = __ldg(prow + j);
+                acc = fmaf(p.x, qq[4 * j], acc);
+                acc = fmaf(p.y, qq[4 * j + 1], acc);
+                acc = fmaf(p.z, qq[4 * j + 2], acc);
+                acc = fmaf(p.w, qq[4 * j + 3], acc);
+            }
+            for (int o = tpr / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (part == 0) qt[i] = acc;
+        }
+        __syncthreads();
+        if constexpr (LUT) {
+            for (int e = threadIdx.x; e < N * LP; e += blockDim.x) {
+                const int n = e / LP, slot = e % LP;
+                const int b = (NB >= 32) ? slot : slot % NB;
+                float c[K];
+                load_codeword<K>(Cs, n, c);
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < K; ++j) acc = fmaf(qt[b * K + j], c[j], acc);
+                Ls[e] = acc;
+            }
+            __syncthreads();
+        }
+    }
+
+    // The lane's query coordinates: k <= 8 without a table: its blocks of q~; k = d: q itself.
+    float qreg[FULL ? D / 32 : (LUT ? 1 : K * SPT)];
+    if constexpr (FULL) {
+#pragma unroll
+        for (int s = 0; s < D / 32; ++s) qreg[s] = qs[s * 32 + lane];
+    } else if constexpr (!LUT) {
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            const int b = (NB >= 32) ? s * 32 + lane : lane % NB;
+#pragma unroll
+            for (int j = 0; j < K; ++j) qreg[s * K + j] = qt[b * K + j];
+        }
+    }
+
     float m = -INFINITY, l = 0.f;
     float z[ZA];
 #pragma unroll
     for (int j = 0; j < ZA; ++j) z[j] = 0.f;
 
-    int64_t tile = tile_lo + warp;
-    if (tile < tile_hi) issue(tile, 0);
     for (int it = 0; tile < tile_hi; ++it, tile += nwarps) {
         const int buf = it & 1;
         if (tile + nwarps < tile_hi) {
@@ -248,13 +277,14 @@ attend_kernel(const AttendArgs a) {
         const int64_t t0 = tile * 32;
         const int nv = T - t0 < 32 ? (int)(T - t0) : 32;
         const int ko = (int)(((kbase + t0) * R) & 31), vo = (int)(((vbase + t0) * R) & 31);
+        const bool one_word = (32 % B == 0) && ((ko | vo) % B == 0);
 
         // Scores.
         float part[NP];
 #pragma unroll
         for (int p = 0; p < NP; ++p) part[p] = 0.f;
         if constexpr (FULL) {
-            const uint32_t my_idx = field(kw, ko + lane * R, mask);
+            const uint32_t my_idx = field<false>(kw, ko + lane * R, mask);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
                 const float *c = a.C + (int64_t)__shfl_sync(0xffffffffu, my_idx, t) * D;
@@ -264,24 +294,28 @@ attend_kernel(const AttendArgs a) {
                 part[t] = acc;
             }
         } else {
+            auto scores = [&](auto one_word) {
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int t = (NB >= 32) ? j / SPT : j * TPS + lane / NB;
                 const int s = (NB >= 32) ? j % SPT : 0;
                 const int b = (NB >= 32) ? s * 32 + lane : lane % NB;
-                const uint32_t idx = field(kw, ko + t * R + b * B, mask);
+                const uint32_t idx = field<decltype(one_word)::value>(kw, ko + t * R + b * B, mask);
                 float v;
                 if constexpr (LUT) {
                     v = Ls[idx * LP + ((NB >= 32) ? b : lane)];
                 } else {
                     float c[K];
-                    load_codeword<K>(Cs + idx * K, c);
+                    load_codeword<K>(Cs, idx, c);
                     v = 0.f;
 #pragma unroll
                     for (int jj = 0; jj < K; ++jj) v = fmaf(qreg[s * K + jj], c[jj], v);
                 }
                 part[(NB >= 32) ? t : j] += v;
             }
+            };
+            if (one_word) scores(std::true_type{});
+            else scores(std::false_type{});
         }
         const float dot = transpose_sum<NP>(part, lane);
         const int tok = (NB >= 32 || FULL) ? lane : (lane % NB) * TPS + lane / NB;
@@ -300,7 +334,7 @@ attend_kernel(const AttendArgs a) {
 
         // Values.
         if constexpr (FULL) {
-            const uint32_t my_idx = field(vw, vo + lane * R, mask);
+            const uint32_t my_idx = field<false>(vw, vo + lane * R, mask);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
                 const float wt = __shfl_sync(0xffffffffu, w, t);
@@ -309,6 +343,7 @@ attend_kernel(const AttendArgs a) {
                 for (int s = 0; s < D / 32; ++s) z[s] = fmaf(wt, __ldg(c + s * 32 + lane), z[s]);
             }
         } else {
+            auto values = [&](auto one_word) {
 #pragma unroll
             for (int j = 0; j < NB; ++j) {
                 const int t = (NB >= 32) ? j / SPT : j * TPS + lane / NB;
@@ -316,12 +351,15 @@ attend_kernel(const AttendArgs a) {
                 const int b = (NB >= 32) ? s * 32 + lane : lane % NB;
                 const int src = (NB >= 32) ? t : (lane / NB) * NB + j;
                 const float wt = __shfl_sync(0xffffffffu, w, src);
-                const uint32_t idx = field(vw, vo + t * R + b * B, mask);
+                const uint32_t idx = field<decltype(one_word)::value>(vw, vo + t * R + b * B, mask);
                 float c[K];
-                load_codeword<K>(Cs + idx * K, c);
+                load_codeword<K>(Cs, idx, c);
 #pragma unroll
                 for (int jj = 0; jj < K; ++jj) z[s * K + jj] = fmaf(wt, c[jj], z[s * K + jj]);
             }
+            };
+            if (one_word) values(std::true_type{});
+            else values(std::false_type{});
         }
         __syncwarp();   // the next issue overwrites this buffer
     }
@@ -383,16 +421,29 @@ attend_kernel(const AttendArgs a) {
         qs[i] = Z / L;
     }
     cluster_sync();   // every CTA's slots have been read; rank 0's qs holds z / sum
-    if (rank == 0 && threadIdx.x < D) {
-        const int j = threadIdx.x;
-        float o;
-        if constexpr (FULL) {
-            o = qs[j];
-        } else {
-            o = 0.f;
-            for (int i = 0; i < D; ++i) o = fmaf(__ldg(a.Pi + (int64_t)i * D + j), qs[i], o);
+    if (rank != 0) return;
+    if constexpr (FULL) {
+        if (threadIdx.x < D) a.out[query * D + threadIdx.x] = qs[threadIdx.x];
+    } else {
+        // o = Pi^T (z / sum): `parts` row ranges per output column, partial sums through wz.
+        int parts = 1;
+        while (parts < 8 && 2 * parts * D <= (int)blockDim.x) parts *= 2;
+        if ((int)threadIdx.x < parts * D) {
+            const int j = threadIdx.x % D, part = threadIdx.x / D, rows = D / parts;
+            float o = 0.f;
+#pragma unroll 8
+            for (int r = 0; r < rows; ++r) {
+                const int i = part * rows + r;
+                o = fmaf(__ldg(a.Pi + (int64_t)i * D + j), qs[i], o);
+            }
+            wz[part * D + j] = o;
         }
-        a.out[query * D + j] = o;
+        __syncthreads();
+        if (threadIdx.x < D) {
+            float o = 0.f;
+            for (int part = 0; part < parts; ++part) o += wz[part * D + threadIdx.x];
+            a.out[query * D + threadIdx.x] = o;
+        }
     }
 }
 
@@ -439,9 +490,10 @@ cudaError_t prepare_attend(fq_ctx *c) {
     const void *fn = select_kernel(c->d, c->k, lut);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    // Largest cluster that can be resident with this shared-memory footprint.
+    // Co-resident CTAs for each cluster size (registers, shared memory and cluster placement all
+    // counted by the runtime's occupancy query); 0 where the size cannot be placed.
     int max_split = 0;
-    for (int s = kMaxSplit; s >= 1 && !max_split; --s) {
+    for (int s = 1; s <= kMaxSplit; ++s) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(s);
         cfg.blockDim = dim3(32 * nwarps);
@@ -456,6 +508,7 @@ cudaError_t prepare_attend(fq_ctx *c) {
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
         if (e != cudaSuccess) return e;
+        c->attend_slots[s] = n * s;
         if (n > 0) max_split = s;
     }
     if (!max_split) return cudaSuccess;
@@ -463,13 +516,10 @@ cudaError_t prepare_attend(fq_ctx *c) {
     c->attend_nwarps = nwarps;
     c->attend_smem = smem;
     c->attend_max_split = max_split;
-    // Co-resident CTAs per SM (228 KB of shared memory, 1 KB reserved per CTA; 64 warps).
-    c->attend_per_sm = std::max(1, std::min((int)(233472 / (smem + 1024)), 64 / nwarps));
     return cudaSuccess;
 }
 
 int attend_split(const fq_ctx *c, int64_t n_queries, int64_t T) {
-    const int64_t slots = (int64_t)c->num_sms * c->attend_per_sm;
     const int64_t n_tiles = (T + 31) / 32;
     // Minimise waves x (tokens per CTA + fixed per-CTA cost in token units).
     const int nb = c->d / c->k;
@@ -477,10 +527,12 @@ int attend_split(const fq_ctx *c, int64_t n_queries, int64_t T) {
     int best = 1;
     double best_cost = 0;
     for (int s = 1; s <= c->attend_max_split && s <= n_tiles; ++s) {
+        const int64_t slots = c->attend_slots[s];
+        if (slots <= 0) continue;
         const int64_t ctas = n_queries * s;
         const double waves = (double)((ctas + slots - 1) / slots);
         const double cost = waves * ((double)T / s + fixed);
-        if (s == 1 || cost < best_cost * 0.98) {
+        if (best_cost == 0 || cost < best_cost * 0.98) {
             best = s;
             best_cost = cost;
         }

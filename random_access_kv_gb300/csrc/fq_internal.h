@@ -34,7 +34,8 @@ struct fq_ctx {
     int kq_max_ctas;
     // fused attention launch shape (attend_nwarps == 0: the configuration does not fit)
     int smem_optin;              // dynamic shared memory a CTA may opt in to
-    int attend_lut, attend_nwarps, attend_max_split, attend_per_sm;
+    int attend_lut, attend_nwarps, attend_max_split;
+    int64_t attend_slots[9];     // co-resident CTAs of the fused attention kernel per cluster size
     size_t attend_smem;
 };
 

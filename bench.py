@@ -17,6 +17,9 @@ attends over all T cached tokens of its group, decoding keys and values inside t
 metric is then cached K/V vectors read per second, and the line carries the attention-output
 cosine against the same attention over the uncompressed fp16 K/V.
 
+`--rate-sweep` measures relative MSE and encode/decode throughput against bits per coordinate,
+through the library, for the scalar Lloyd-Max codec (k = 1) and FibQuant at k = 2, 4, 8 and d.
+
 `--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
 sample of the same workload instead.
 
@@ -655,6 +658,85 @@ def run_attend(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+# Rate sweep: (codec, k, N) points at d = 64; b = log2(N) / k bits per coordinate.
+SWEEP_POINTS = ([("scalar", 1, n) for n in (2, 4, 8, 16)]
+                + [("fibquant", 2, n) for n in (4, 8, 16, 32, 64, 128, 256)]
+                + [("fibquant", 4, n) for n in (16, 64, 256, 1024, 4096)]
+                + [("fibquant", 8, n) for n in (256, 4096)]
+                + [("fibquant", 64, n) for n in (256, 1024, 4096)])
+
+
+def run_rate_sweep(args) -> None:
+    """Relative MSE and kernel throughput against bits per coordinate, through the library, for the
+    scalar Lloyd-Max codec (k = 1, integer rates only) and FibQuant at k = 2, 4, 8 and d."""
+    import torch
+    import random_access_kv_gb300 as fq
+    from random_access_kv_gb300 import build as fbuild
+    from random_access_kv_gb300 import codebook as pcb
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fbuild.build()
+    d, rows, seed = 64, args.rows or 262144, 1
+    Pi = pcb.haar(synth.rotation_gaussian(seed, d)).astype(np.float32)
+    x_np = synth.gaussian_rows(seed, 3, rows, d)
+    x = torch.from_numpy(x_np).to(dev)
+    x64 = x.double()
+    xx = (x64 * x64).sum(dim=1)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    points = []
+    for i, (codec, k, N) in enumerate(SWEEP_POINTS):
+        t0 = time.perf_counter()
+        if codec == "scalar":
+            C, _ = pcb.scalar_lloyd_max(d, N)
+        else:
+            kind = "sphere" if k == d else ("spiral" if k == 2 else "kronecker")
+            T = int(min(131072, max(32768, 32 * N)))
+            C, _ = pcb.build(kind, d, k, N, synth.source_gaussians(seed, T, d, chunk=100 + i), 10)
+        build_s = time.perf_counter() - t0
+        ctx = fq.fq_codebook_load(C.astype(np.float32), Pi, local)
+        nu, codes = fq.alloc_store(ctx, rows, dev)
+        out = torch.empty((rows, d), dtype=torch.float16, device=dev)
+        enc_ms, dec_ms = [], []
+        for rep in range(3 + args.steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            flush.zero_()
+            ev[0].record(stream)
+            fq.fq_encode(ctx, x, rows, nu, codes, 0, sp)
+            ev[1].record(stream)
+            fq.fq_decode(ctx, nu, codes, rows, out, sp)
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            if rep >= 3:
+                enc_ms.append(ev[0].elapsed_time(ev[1]))
+                dec_ms.append(ev[1].elapsed_time(ev[2]))
+        err = ((out.double() - x64) ** 2).sum(dim=1)
+        mse = float((err / xx).mean())
+        flags = fq.fq_status(ctx, sp)
+        R = fq.fq_record_bits(ctx)
+        points.append({"codec": codec, "k": k, "N": N, "bits_per_coordinate": round(np.log2(N) / k, 4),
+                       "record_bits": R, "relative_mse": mse,
+                       "encode_vectors_per_s": rows / (statistics.median(enc_ms) / 1e3),
+                       "decode_vectors_per_s": rows / (statistics.median(dec_ms) / 1e3),
+                       "codebook_build_s": round(build_s, 2), "device_flags": flags})
+        ctx.close()
+        del nu, codes, out
+    line = {"metric": "relative MSE E|x - x_hat|^2 / |x|^2 by bits per coordinate", "unit": "ratio",
+            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{rows} N(0,1) fp16 rows, d = {d}, one shared Haar rotation",
+                       "codebooks": "scalar: exact Lloyd-Max on the rotated-coordinate law; fibquant: "
+                                    "radial-angular initialisation + 10 Lloyd iterations on "
+                                    "max(32768, min(131072, 32 N)) source draws",
+                       "timing": "median of steps launches, L2 flushed before each encode"},
+            "points": points}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -664,6 +746,8 @@ def main():
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--attend", action="store_true", help="time fused decode-into-attention")
+    ap.add_argument("--rate-sweep", action="store_true",
+                    help="relative MSE and throughput against bits per coordinate (scalar k = 1 vs FibQuant)")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --attend: the first G (layer, head) groups only (a small case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -675,6 +759,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.rate_sweep:
+        run_rate_sweep(args)
     elif args.attend:
         run_attend(args)
     else:

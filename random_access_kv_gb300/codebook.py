@@ -15,6 +15,10 @@ vector quantisation for random-access KV-cache compression":
             vector over its norm); restart r >= 1 rotates the start by a k x k Haar matrix; the
             lowest training MSE wins.
 
+The scalar comparison codec of [FibQuant §1] (normalise, rotate, then quantise every rotated
+coordinate with one scalar Lloyd-Max table) is the k = 1 case of the same interface; its table is
+``scalar_lloyd_max``.
+
 This is construction-time code, not part of the encode/decode path.
 """
 from __future__ import annotations
@@ -111,6 +115,49 @@ def build(kind: str, d: int, k: int, N: int, train_gaussians: np.ndarray, iters:
         if cand[1] < best[1]:
             best = cand
     return best
+
+
+def scalar_lloyd_max(d: int, N: int, tol: float = 1e-13, max_iter: int = 200000) -> tuple[np.ndarray, float]:
+    """Scalar Lloyd-Max table for one coordinate y of a Haar-uniform unit d-vector: (levels
+    ascending as C [N, 1], per-coordinate MSE). The density of y is proportional to
+    (1 - y^2)^m, m = (d - 3)/2, on [-1, 1] (y^2 ~ Beta(1/2, (d - 1)/2)). Lloyd-Max alternates
+    midpoint thresholds and cell centroids; cell masses use the regularised incomplete beta
+    function and cell first moments the closed form of the integral of y (1 - y^2)^m. The density
+    is log-concave, so the fixed point is unique."""
+    if d < 3 or N < 1:
+        raise ValueError("need d >= 3 and N >= 1")
+    a, b = 0.5, 0.5 * (d - 1)
+    m = 0.5 * (d - 3)
+    norm = np.exp(special.betaln(a, b))           # integral of (1 - y^2)^m over [-1, 1]
+
+    def half_mass(y):                             # P(0 <= Y <= |y|), without cancellation near 1
+        return 0.5 * special.betainc(a, b, np.minimum(y * y, 1.0))
+
+    def mass(lo, hi):
+        both_pos, both_neg = lo >= 0, hi <= 0
+        out = np.sign(hi) * half_mass(hi) - np.sign(lo) * half_mass(lo)
+        # cells on one side: difference of upper-tail masses
+        tail = lambda y: 0.5 * special.betaincc(a, b, np.minimum(y * y, 1.0))
+        out = np.where(both_pos, tail(lo) - tail(hi), out)
+        out = np.where(both_neg, tail(hi) - tail(lo), out)
+        return out
+
+    def moment(lo, hi):                           # integral of y f(y) over [lo, hi]
+        return (np.power(1.0 - lo * lo, m + 1.0) - np.power(1.0 - hi * hi, m + 1.0)) / (2.0 * (m + 1.0) * norm)
+
+    q = (np.arange(N, dtype=np.float64) + 0.5) / N
+    c = np.sign(q - 0.5) * np.sqrt(special.betaincinv(a, b, np.abs(2.0 * q - 1.0)))
+    for _ in range(max_iter):
+        t = np.concatenate([[-1.0], 0.5 * (c[1:] + c[:-1]), [1.0]])
+        P = mass(t[:-1], t[1:])
+        new = moment(t[:-1], t[1:]) / P
+        done = np.max(np.abs(new - c)) <= tol
+        c = new
+        if done:
+            break
+    t = np.concatenate([[-1.0], 0.5 * (c[1:] + c[:-1]), [1.0]])
+    mse = 1.0 / d - float(np.sum(mass(t[:-1], t[1:]) * c * c))
+    return c[:, None], mse
 
 
 def for_workload(cfg: int) -> tuple[np.ndarray, np.ndarray]:

@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (tid == 0) {
-        const uint32_t cb_bytes = CB_SMEM ? (uint32_t)(p.N * K * 4) : 0u;
+        // A bulk copy moves a multiple of 16 bytes; the table is allocated padded to one.
+        const uint32_t cb_bytes = CB_SMEM ? ((uint32_t)(p.N * K * 4) + 15u) & ~15u : 0u;
         mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + cb_bytes);
         bulk_g2s(sm + L::oPi, p.pit_split, 2u * L::kPiPart, bar_tab);
         if (CB_SMEM) bulk_g2s(sm + L::oCb, p.cb, cb_bytes, bar_tab);
@@ -350,7 +351,10 @@ cudaError_t prepare_decode_tc(fq_ctx *ctx) {
         }
     e = cudaMalloc((void **)&ctx->pit_split, pts.size() * 2);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->pit_split, pts.data(), pts.size() * 2, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->cb_split, cb.size() * 2);
+    // Padded to a multiple of 16 bytes: the kernel bulk-copies the whole table (N k = 2 gives 8 bytes).
+    const size_t cb_alloc = (cb.size() * 2 + 15) & ~(size_t)15;
+    if (e == cudaSuccess) e = cudaMalloc((void **)&ctx->cb_split, cb_alloc);
+    if (e == cudaSuccess) e = cudaMemset(ctx->cb_split, 0, cb_alloc);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->cb_split, cb.data(), cb.size() * 2, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return e;
     {

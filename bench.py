@@ -9,7 +9,9 @@ address packing), then random-access decode of 65,536 uniformly drawn rows from 
 (gather, unpack, codeword lookup, inverse rotation, scaling). K and V share the codebook and
 live in one code store, so each step is one encode launch and one gather launch. Inputs are resident in HBM when
 the timed region starts; L2 is flushed (a 256 MB write) before every timed step, outside the
-step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it.
+step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it. A step's
+events bracket both launches (the decode is launched as a programmatic dependent of the encode);
+the roofline's per-kernel times come from each launch timed on its own, L2 flushed before it.
 
 `--attend` times fused decode-into-attention instead: the workload's K and V are encoded into one
 store (untimed), then each step is one launch in which one fp16 query per (layer, head) group
@@ -324,22 +326,41 @@ def run_ours(args) -> None:
     enc_launches = n_steps if streaming else 1
     launches_per_step = enc_launches + 1
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def encode_all():
         if streaming:
             for st in range(n_steps):
                 fq.fq_encode_append(ctx, xs[st], nt * n_seq, new, T, st * new, nu, codes, sp)
         else:
             fq.fq_encode(ctx, xs, MT, nu, codes, 0, sp)
-        if ev is not None:
-            ev[1].record(stream)
+
+    def decode_all():
         if gathers:
             fq.fq_decode_gather(ctx, nu, codes, MT, idx, G, out, sp)
         else:
             fq.fq_decode(ctx, nu, codes, MT, out, sp)
+
+    def step(ev=None):
+        # No event between the launches: each kernel lets the next one be scheduled before it
+        # ends (programmatic dependent launch), and an event in between would serialise them.
         if ev is not None:
-            ev[2].record(stream)
+            ev[0].record(stream)
+        encode_all()
+        decode_all()
+        if ev is not None:
+            ev[1].record(stream)
+
+    def timed_alone(fn, reps):
+        """Per-kernel device time: fn bracketed by its own events, L2 flushed before each."""
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(a.elapsed_time(b))
+        return ms
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -356,17 +377,18 @@ def run_ours(args) -> None:
     sampler.start()
     for _ in range(args.steps):
         flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         step(ev)
         evs.append(ev)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
-    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
-    enc_step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_step_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = sum(step_ms)
+    # Per-kernel times for the roofline, each launch timed on its own.
+    enc_step_ms = timed_alone(encode_all, max(3, args.steps))
+    dec_step_ms = timed_alone(decode_all, max(3, args.steps))
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)

@@ -47,6 +47,7 @@ void free_ctx(fq_ctx *c) {
     cudaFree(c->grid2);
     cudaFree(c->pit_split);
     cudaFree(c->cb_split);
+    cudaFree(c->cb_lanes);
     cudaFree(c->crot_split);
     cudaFree(c->cb_ops);
     free(c);
@@ -216,7 +217,7 @@ int fq_encode_append(fq_ctx *ctx, const void *x, int64_t n_seq, int64_t n_new, i
 
 static int decode_common(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M,
                          const int64_t *idx, int64_t n, void *out, bool out_f32, void *stream) {
-    if (!ctx || M < 0 || n < 0) return FQ_EINVAL;
+    if (!ctx || M < 0 || n < 0 || n > INT32_MAX) return FQ_EINVAL;
     if (n == 0) return FQ_OK;
     if (!out || (!idx && n > M)) return FQ_EINVAL;
     if (M > 0 && (!nu || !codes)) return FQ_EINVAL;

@@ -9,8 +9,11 @@
 //   2. One thread issues Y_hat Pi on the tensor pipe as three fp16 MMAs into a TMEM fp32
 //      accumulator: hi*Pi_hi + hi*Pi_lo + lo*Pi_hi, with Pi^T carried as fp16 halves of 2^12 Pi^T
 //      (the dropped lo*lo term is below 2^-22 of the result).
-//   3. Each thread reads its row back, scales it by nu 2^-22 and stores it (fp16 rounded to
-//      nearest even, or fp32).
+//   3. Each thread reads its row back and scales it by nu 2^-22. fp16 output (rounded to nearest
+//      even) is staged row by row in the tile's A buffer, in the same 128-byte swizzle, and
+//      written by one TMA tensor store per 64-column box; fp32 output is stored row by row.
+// With d = 64 and a codebook of at most 512 words (k <= 2), the table is held once per lane
+// (word w of lane l at w * 32 + l), so that the random codeword reads of a warp never share a bank.
 // Gather indices outside [0, M) give zero rows and set FQ_FLAG_RANGE.
 #include <math.h>
 #include <string.h>
@@ -32,14 +35,17 @@ constexpr float kPiScale = 4096.f;    // 2^12 on Pi^T
 constexpr float kYScale = 1024.f;     // 2^10 on the codewords
 constexpr float kOutScale = 1.0f / (4096.f * 1024.f);
 
-template <int D, int K, int NG, bool CB_SMEM>
+// Where the codebook halves are read from.
+constexpr int kCbGlobal = 0, kCbShared = 1, kCbLanes = 2;
+
+template <int D, int K, int NG, int CBM>
 struct DLayout {
     static constexpr int kPiPart = D * D * 2;
     static constexpr int kATile = kTileRows * D * 2;                 // one fp16 A operand
     static constexpr int oPi = 0;
     static constexpr int oA = oPi + 2 * kPiPart;
     static constexpr int oCb = oA + NG * 2 * kATile;
-    static constexpr int kCbMax = CB_SMEM ? 16384 : 0;
+    static constexpr int kCbMax = CBM == kCbShared ? 16384 : CBM == kCbLanes ? 65536 : 0;
     static constexpr int oBar = oCb + kCbMax;
     static constexpr int kBars = 1 + NG;
     static constexpr int oTmem = oBar + kBars * 8;
@@ -57,6 +63,7 @@ struct DecParams {
     int N;
     const uint8_t *pit_split; // [2][D*D] fp16 halves of 2^12 Pi^T, swizzled
     const uint16_t *cb;       // [N][2K] fp16: K hi halves then K lo halves of 2^10 c_n
+    const uint32_t *cb_lanes; // the words of cb, each repeated for the 32 lanes (or null)
     void *out;
     uint32_t *flags;
 };
@@ -67,9 +74,21 @@ struct CwHalves {
     uint32_t hi[K > 1 ? K / 2 : 1], lo[K > 1 ? K / 2 : 1];
 };
 
-template <int K, bool CB_SMEM>
-__device__ __forceinline__ CwHalves<K> fetch_cw(const uint16_t *cb, uint32_t n) {
+template <int K, int CBM>
+__device__ __forceinline__ CwHalves<K> fetch_cw(const uint16_t *cb, uint32_t n, int lane) {
     CwHalves<K> r;
+    constexpr bool CB_SMEM = CBM == kCbShared;
+    if constexpr (CBM == kCbLanes) {
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(cb) + lane;
+        if constexpr (K == 2) {
+            r.hi[0] = w[(2 * n) * 32];
+            r.lo[0] = w[(2 * n + 1) * 32];
+        } else {
+            const uint32_t v = w[n * 32];
+            r.hi[0] = v & 0xFFFFu; r.lo[0] = v >> 16;
+        }
+        return r;
+    }
     const uint16_t *p = cb + (size_t)n * 2 * K;
     if constexpr (K == 8) {
         const uint4 h = CB_SMEM ? *reinterpret_cast<const uint4 *>(p) : __ldg(reinterpret_cast<const uint4 *>(p));
@@ -155,9 +174,11 @@ __device__ __forceinline__ uint32_t field(const uint32_t (&w)[W], int b) {
     return v & ((1u << BS) - 1u);
 }
 
-template <int D, int K, int NG, bool CB_SMEM, int BS, typename OutT>
-__global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
-    using L = DLayout<D, K, NG, CB_SMEM>;
+template <int D, int K, int NG, int CBM, int BS, typename OutT>
+__global__ void __launch_bounds__(NG * 128, 1) decode_tc(const __grid_constant__ CUtensorMap omap, const DecParams p) {
+    constexpr bool CB_SMEM = CBM != kCbGlobal;
+    constexpr bool TMA_OUT = sizeof(OutT) == 2;
+    using L = DLayout<D, K, NG, CBM>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -178,9 +199,6 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
     const int64_t first = (int64_t)blockIdx.x * NG + g;
     constexpr int W = BS ? (D / K) * BS / 32 : 0;
 
-    // The first tile's row data is requested before the tables arrive.
-    RowData<W> cur = load_row<D, K, BS>(p, first, t);
-
     if (tid == 0) {
         for (int i = 0; i < L::kBars; ++i) mbar_init(bars + i, 1);
         fence_barrier_init();
@@ -191,11 +209,20 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
     const uint32_t tmem_base = *tmem_slot;
     if (tid == 0) {
         // A bulk copy moves a multiple of 16 bytes; the table is allocated padded to one.
-        const uint32_t cb_bytes = CB_SMEM ? ((uint32_t)(p.N * K * 4) + 15u) & ~15u : 0u;
+        const uint32_t cb_bytes = CBM == kCbLanes ? (uint32_t)(p.N * K * 4 * 32)
+                                  : CB_SMEM ? ((uint32_t)(p.N * K * 4) + 15u) & ~15u : 0u;
         mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart + cb_bytes);
         bulk_g2s(sm + L::oPi, p.pit_split, 2u * L::kPiPart, bar_tab);
-        if (CB_SMEM) bulk_g2s(sm + L::oCb, p.cb, cb_bytes, bar_tab);
+        if (CB_SMEM)
+            bulk_g2s(sm + L::oCb, CBM == kCbLanes ? static_cast<const void *>(p.cb_lanes) : static_cast<const void *>(p.cb),
+                     cb_bytes, bar_tab);
+        if (TMA_OUT) prefetch_tensormap(&omap);
     }
+    // Indices, norms and codes may be written by the previous kernel in the stream.
+    griddep_launch_dependents();
+    griddep_wait();
+    // The first tile's row data is requested before the tables arrive.
+    RowData<W> cur = load_row<D, K, BS>(p, first, t);
     bool ok = named_sync_and(1 + g, 128, mbar_wait(bar_tab, 0));
 
     constexpr int NB = D / K;
@@ -222,7 +249,7 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
                     uint32_t i;
                     if constexpr (BS != 0) i = field<BS, W>(cur.w, c * BPC + b);
                     else i = rd.get(p.B);
-                    const CwHalves<K> v = fetch_cw<K, CB_SMEM>(cb, i);
+                    const CwHalves<K> v = fetch_cw<K, CBM>(cb, i, t & 31);
                     if constexpr (K >= 2) {
 #pragma unroll
                         for (int q = 0; q < K / 2; ++q) {
@@ -261,18 +288,51 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const DecParams p) {
         ok = named_sync_and(1 + g, 128, mbar_wait(bar_mma, (uint32_t)(it & 1)));
         if (!ok) break;
         tc_fence_after();
+        if constexpr (TMA_OUT) {
+            // Row t of the output tile into the A buffer the MMA has finished with, then one
+            // tensor store per 64-column box (rows past n are clipped by the store).
 #pragma unroll 1
-        for (int c = 0; c < D / 16; ++c) {
-            float v[16];
-            tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), v);
-            tmem_wait_ld();
-            if (cur.live) store16<D, OutT>(out, cur.j, c, v, cur.s);
+            for (int c = 0; c < D / 16; ++c) {
+                float v[16];
+                tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), v);
+                tmem_wait_ld();
+                uint32_t w[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const __half2 h = __floats2half2_rn(v[2 * q] * cur.s, v[2 * q + 1] * cur.s);
+                    w[q] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int ch = 2 * c + hh, kb = ch / 8, cc = ch % 8;
+                    const uint32_t off = (uint32_t)(kb * 16384 + t * 128 + ((cc ^ (t & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(a_hi + off) = make_uint4(w[4 * hh], w[4 * hh + 1], w[4 * hh + 2], w[4 * hh + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_sync(1 + g, 128);
+            if (t == 0) {
+#pragma unroll
+                for (int kb = 0; kb < D / 64; ++kb) tma_store_2d(&omap, a_hi + kb * 16384, kb * 64, (int)(tile * kTileRows));
+                bulk_commit();
+                bulk_wait_read0();          // the next tile's A operand overwrites this buffer
+            }
+        } else {
+#pragma unroll 1
+            for (int c = 0; c < D / 16; ++c) {
+                float v[16];
+                tmem_ld16(tmem_acc + ((uint32_t)(32 * wq) << 16) + (uint32_t)(16 * c), v);
+                tmem_wait_ld();
+                if (cur.live) store16<D, OutT>(out, cur.j, c, v, cur.s);
+            }
+            tc_fence_before();
         }
-        tc_fence_before();
         named_sync(1 + g, 128);
         cur = nxt;
     }
     if (!ok && t == 0) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+    if (TMA_OUT && t == 0) bulk_wait_all();   // stores complete before the CTA's memory goes away
     __syncthreads();
     if (!ok) mbar_wait(bar_mma, 0, 1000000ull);
     tc_fence_after();
@@ -283,31 +343,59 @@ template <int D, int K>
 constexpr int groups() { return D == 64 ? 4 : 2; }
 
 template <int D, int K>
-constexpr bool cb_in_smem() { return K <= 4; }
+constexpr int cb_mode() { return K <= 4 ? kCbShared : kCbGlobal; }
 
-template <int D, int K, int BS, typename OutT>
-cudaError_t launch_dk(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
+// The lane-replicated table fits its 64 KB slot beside four d = 64 row groups.
+template <int D, int K>
+constexpr bool lanes_possible() { return D == 64 && K <= 2; }
+
+template <int D, int K, int CBM, int BS, typename OutT>
+cudaError_t launch_dkm(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
     constexpr int NG = groups<D, K>();
-    constexpr bool CBS = cb_in_smem<D, K>();
-    using L = DLayout<D, K, NG, CBS>;
+    using L = DLayout<D, K, NG, CBM>;
+    CUtensorMap omap;
+    memset(&omap, 0, sizeof(omap));
+    if (sizeof(OutT) == 2 && !encode_rows_tensor_map(&omap, p.out, p.n, D)) return cudaErrorInvalidValue;
     const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
     int64_t grid = (ntiles + NG - 1) / NG;
     if (grid > ctx->num_sms) grid = ctx->num_sms;
-    decode_tc<D, K, NG, CBS, BS, OutT><<<(unsigned)grid, NG * 128, L::kBytes, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NG * 128);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc<D, K, NG, CBM, BS, OutT>, omap, p);
+}
+
+template <int D, int K, int BS, typename OutT>
+cudaError_t launch_dk(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
+    if constexpr (lanes_possible<D, K>())
+        if (p.cb_lanes) return launch_dkm<D, K, kCbLanes, BS, OutT>(ctx, p, s);
+    return launch_dkm<D, K, cb_mode<D, K>(), BS, OutT>(ctx, p, s);
+}
+
+template <int D, int K, int CBM, int BS>
+cudaError_t prep_dkm() {
+    constexpr int NG = groups<D, K>();
+    using L = DLayout<D, K, NG, CBM>;
+    static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(decode_tc<D, K, NG, CBM, BS, __half>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(decode_tc<D, K, NG, CBM, BS, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                L::kBytes);
 }
 
 template <int D, int K, int BS>
-cudaError_t prep_dk() {
-    constexpr int NG = groups<D, K>();
-    constexpr bool CBS = cb_in_smem<D, K>();
-    using L = DLayout<D, K, NG, CBS>;
-    static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
-    cudaError_t e = cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, BS, __half>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(decode_tc<D, K, NG, CBS, BS, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                L::kBytes);
+cudaError_t prep_dk(bool lanes) {
+    if constexpr (lanes_possible<D, K>())
+        if (lanes) return prep_dkm<D, K, kCbLanes, BS>();
+    return prep_dkm<D, K, cb_mode<D, K>(), BS>();
 }
 
 // Record widths with a compile-time field size: (d, k, B) of the synthetic workloads, whose
@@ -357,15 +445,26 @@ cudaError_t prepare_decode_tc(fq_ctx *ctx) {
     if (e == cudaSuccess) e = cudaMemset(ctx->cb_split, 0, cb_alloc);
     if (e == cudaSuccess) e = cudaMemcpy(ctx->cb_split, cb.data(), cb.size() * 2, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return e;
+    // Lane-replicated copy of the table's 32-bit words (d = 64, k <= 2, N k <= 512 words).
+    const bool lanes = d == 64 && k <= 2 && (size_t)N * k <= 512;
+    if (lanes) {
+        std::vector<uint32_t> words((size_t)N * k), rep((size_t)N * k * 32);
+        memcpy(words.data(), cb.data(), words.size() * 4);
+        for (size_t w = 0; w < words.size(); ++w)
+            for (int l = 0; l < 32; ++l) rep[w * 32 + l] = words[w];
+        e = cudaMalloc((void **)&ctx->cb_lanes, rep.size() * 4);
+        if (e == cudaSuccess) e = cudaMemcpy(ctx->cb_lanes, rep.data(), rep.size() * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return e;
+    }
     {
         cudaError_t es = cudaSuccess;
-        if (static_bits(d, k, ctx->B) == 4) es = prep_dk<64, 2, 4>();
-        if (static_bits(d, k, ctx->B) == 8) es = prep_dk<64, 2, 8>();
-        if (static_bits(d, k, ctx->B) == 10) es = prep_dk<64, 4, 10>();
-        if (static_bits(d, k, ctx->B) == 12) es = prep_dk<128, 8, 12>();
+        if (static_bits(d, k, ctx->B) == 4) es = prep_dk<64, 2, 4>(lanes);
+        if (static_bits(d, k, ctx->B) == 8) es = prep_dk<64, 2, 8>(lanes);
+        if (static_bits(d, k, ctx->B) == 10) es = prep_dk<64, 4, 10>(lanes);
+        if (static_bits(d, k, ctx->B) == 12) es = prep_dk<128, 8, 12>(lanes);
         if (es != cudaSuccess) return es;
     }
-#define PREP(D, K) prep_dk<D, K, 0>()
+#define PREP(D, K) prep_dk<D, K, 0>(lanes)
     if (d == 64) {
         if (k == 1) return PREP(64, 1);
         if (k == 2) return PREP(64, 2);
@@ -391,6 +490,7 @@ cudaError_t launch_decode_tc(const fq_ctx *ctx, const float *nu, const uint32_t 
     p.N = ctx->N;
     p.pit_split = ctx->pit_split;
     p.cb = ctx->cb_split;
+    p.cb_lanes = ctx->cb_lanes;
     p.out = out;
     p.flags = ctx->flags;
 #define CALLB(D, K, BS) (out_f32 ? launch_dk<D, K, BS, float>(ctx, p, s) : launch_dk<D, K, BS, __half>(ctx, p, s))

@@ -212,6 +212,9 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         slice(grid, p.tables, tab_bytes, bar_grid);
         slice(cw, p.cw, cw_bytes, bar_grid);
     }
+    // Tables are in flight; x and the outputs may belong to the previous kernel in the stream.
+    griddep_launch_dependents();
+    griddep_wait();
     // Each row group's first x tile.
     if (t == 0 && first < ntiles) {
         mbar_arrive_expect_tx(bar_load, (uint32_t)L::kXTile);
@@ -401,13 +404,15 @@ cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     cfg.blockDim = dim3(NG * 128);
     cfg.dynamicSmemBytes = L::kBytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, encode_k2_tc<D, NG, NBUF, BS>, tm, p);
 }
 

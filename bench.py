@@ -22,6 +22,9 @@ cosine against the same attention over the uncompressed fp16 K/V.
 `--rate-sweep` measures relative MSE and encode/decode throughput against bits per coordinate,
 through the library, for the scalar Lloyd-Max codec (k = 1) and FibQuant at k = 2, 4, 8 and d.
 
+`--lloyd` times the workload's codebook construction: host numpy Lloyd against GPU Lloyd (the
+library's encoder assigns, `fq_centroid_sums` forms the centroids).
+
 `--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
 sample of the same workload instead.
 
@@ -68,8 +71,9 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured",
+                "sms": 152}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback", "sms": 152}
 
 
 # The source file of each timed kernel; its hash (with the shared headers) ties a committed ncu
@@ -467,6 +471,18 @@ def run_ours(args) -> None:
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         roofline.update({"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4)})
+    if w.k < w.d:
+        # The other bound of a k <= 8 encode: an exhaustive nearest-codeword search on the CUDA
+        # cores, (d/k) N (k + 2) lane instructions per row, against 128 lane instructions per
+        # cycle per SM at the sampled clock. Above 1.0 means the search beats exhaustive scanning.
+        instr = (d // w.k) * w.N * (w.k + 2)
+        sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+        alu_peak = peaks["sms"] * 128 * sm_mhz * 1e6
+        enc_rows_s = enc_rows / (enc_ms / 1e3)
+        roofline["search_alu"] = {"bound": "alu", "instr_per_row": instr,
+                                  "achieved": round(enc_rows_s * instr / 1e12, 2),
+                                  "peak": round(alu_peak / 1e12, 2), "unit": "T lane-instr/s",
+                                  "frac": round(enc_rows_s * instr / alu_peak, 3)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -759,6 +775,67 @@ def run_rate_sweep(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_lloyd(args) -> None:
+    """Codebook building for one workload's (kind, d, k, N) and Lloyd budget: the host builder
+    (numpy) against the GPU builder (library encoder + fq_centroid_sums), on the same number of
+    block draws and on 16 times as many; each codebook's distortion on held-out rows."""
+    import torch
+    import random_access_kv_gb300 as fq
+    from random_access_kv_gb300 import build as fbuild
+    from random_access_kv_gb300 import codebook as pcb
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fbuild.build()
+    cfg = args.workload
+    w = synth.WORKLOADS[cfg]
+    d, k, N = w.d, w.k, w.N
+    s = synth.kronecker_offset(cfg)
+    restarts = [synth.restart_gaussian(cfg, k, r) for r in range(1, w.lloyd_restarts)]
+    nb = d // k
+    # held-out rows: every block of a row over its norm is a draw of the block source (identity rotation)
+    X_test = torch.from_numpy(synth.source_gaussians(cfg, 65536, d, chunk=9).astype(np.float16)).to(dev)
+    eye = np.eye(d, dtype=np.float32)
+
+    def heldout(C):
+        ctx = fq.fq_codebook_load(C.astype(np.float32), eye, local)
+        T = X_test.shape[0]
+        nu, codes = fq.alloc_store(ctx, T, dev)
+        fq.fq_encode(ctx, X_test, T, nu, codes)
+        out = torch.empty((T, d), dtype=torch.float32, device=dev)
+        fq.fq_decode_gather_f32(ctx, nu, codes, T, torch.arange(T, device=dev), T, out)
+        x = X_test.double()
+        rel = ((out.double() - x) ** 2).sum(dim=1) / (x * x).sum(dim=1)
+        ctx.close()
+        return float(rel.mean()) / nb
+
+    points = []
+    t0 = time.perf_counter()
+    C, mse = pcb.build(w.codebook_kind, d, k, N, synth.source_gaussians(cfg, w.lloyd_train, d), w.lloyd_iters,
+                       restarts, s)
+    points.append({"builder": "host numpy", "block_draws": w.lloyd_train, "seconds": round(time.perf_counter() - t0, 3),
+                   "train_mse": mse, "heldout_mse": heldout(C)})
+    for mult in (1, 16):
+        rows = -(-w.lloyd_train * mult // nb)
+        X = synth.source_gaussians(cfg, rows, d, chunk=1).astype(np.float16)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        C, mse = pcb.build_gpu(w.codebook_kind, d, k, N, X, w.lloyd_iters, restarts, s, device=local)
+        torch.cuda.synchronize(dev)
+        points.append({"builder": "gpu", "block_draws": rows * nb, "seconds": round(time.perf_counter() - t0, 3),
+                       "train_mse": mse, "heldout_mse": heldout(C)})
+    line = {"metric": "codebook build seconds and per-block distortion, host vs GPU Lloyd", "unit": "s",
+            "higher_is_better": False, "n_gpus": 1, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "kind": w.codebook_kind, "d": d, "k": k, "N": N,
+                       "lloyd_iters": w.lloyd_iters, "restarts": w.lloyd_restarts,
+                       "heldout": "65,536 rows, all d/k blocks each (identity rotation)"},
+            "points": points}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -770,6 +847,8 @@ def main():
     ap.add_argument("--attend", action="store_true", help="time fused decode-into-attention")
     ap.add_argument("--rate-sweep", action="store_true",
                     help="relative MSE and throughput against bits per coordinate (scalar k = 1 vs FibQuant)")
+    ap.add_argument("--lloyd", action="store_true",
+                    help="codebook building: host numpy Lloyd against the GPU Lloyd for --workload")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --attend: the first G (layer, head) groups only (a small case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -783,6 +862,8 @@ def main():
         run_reference(args)
     elif args.rate_sweep:
         run_rate_sweep(args)
+    elif args.lloyd:
+        run_lloyd(args)
     elif args.attend:
         run_attend(args)
     else:

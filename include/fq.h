@@ -149,6 +149,21 @@ int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, co
               int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,
               int64_t stride, float scale, float *out, void *stream);
 
+/*
+ * fq_centroid_sums - the centroid step of a Lloyd iteration on the codebook [FibQuant §2.2,
+ * refinement: Lloyd iterations on draws of the block source minimise the finite codebook's MSE].
+ * The assignment step is fq_encode of the training rows; this call then adds, for every codeword n,
+ *   sums[n][0..k) += sum of the blocks u_b (u = Pi x / nu) whose index is n,
+ *   counts[n]     += their number,
+ * over rows m < M. Rows with nu = 0 are skipped.
+ *   x      : device fp16 [M x d], the encoded rows, 16-byte aligned;
+ *   nu, codes : the store fq_encode wrote for exactly these rows (row m at record m);
+ *   sums   : device float64 [N x k], counts : device float64 [N], accumulated (the caller zeroes).
+ * The new codebook is sums[n] / counts[n] wherever counts[n] > 0.
+ */
+int fq_centroid_sums(fq_ctx *ctx, const void *x, int64_t M, const float *nu, const uint32_t *codes,
+                     double *sums, double *counts, void *stream);
+
 /* Number of uint32 words of a store of M records: ceil(M R / 32). Returns -1 on bad arguments. */
 int64_t fq_code_words(const fq_ctx *ctx, int64_t M);
 

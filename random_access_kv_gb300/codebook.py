@@ -13,7 +13,9 @@ vector quantisation for random-access KV-cache compression":
             normalised; phi_k solves x^(k+1) = x + 1. k = d: the unit directions alone.
   Lloyd     multi-restart Lloyd on draws of the block source (first k coordinates of a Gaussian
             vector over its norm); restart r >= 1 rotates the start by a k x k Haar matrix; the
-            lowest training MSE wins.
+            lowest training MSE wins. ``build_gpu`` runs the same iterations through the library:
+            the encoder assigns every block of every training row, ``fq_centroid_sums`` forms
+            the centroids.
 
 The scalar comparison codec of [FibQuant §1] (normalise, rotate, then quantise every rotated
 coordinate with one scalar Lloyd-Max table) is the k = 1 case of the same interface; its table is
@@ -112,6 +114,63 @@ def build(kind: str, d: int, k: int, N: int, train_gaussians: np.ndarray, iters:
     best = refine(C0, Y, iters)
     for G in restart_gaussians:
         cand = refine(C0 @ haar(G).T, Y, iters)
+        if cand[1] < best[1]:
+            best = cand
+    return best
+
+
+def refine_gpu(C: np.ndarray, X, iters: int, rtol: float = 1e-6, device: int = 0) -> tuple[np.ndarray, float]:
+    """``refine`` on the GPU. X: fp16 training rows [T, d] on the device; with the identity
+    rotation every d/k block of a row, over the row's norm, is one draw of the block source. Each
+    iteration is one library encode (the assignment: nearest codeword of every block) and one
+    ``fq_centroid_sums`` (the centroid step); the distortion of the current codebook comes from the
+    same sums: mean |u_b - c|^2 = (rows - 2 sum_n s_n.c_n + sum_n m_n |c_n|^2) / blocks."""
+    import torch
+
+    import random_access_kv_gb300 as fq
+    C = np.array(C, dtype=np.float64, copy=True)
+    N, k = C.shape
+    T, d = X.shape
+    eye = np.eye(d, dtype=np.float32)
+    sums = torch.zeros((N, k), dtype=torch.float64, device=X.device)
+    counts = torch.zeros(N, dtype=torch.float64, device=X.device)
+
+    def assign(C):
+        ctx = fq.fq_codebook_load(C.astype(np.float32), eye, device)
+        nu, codes = fq.alloc_store(ctx, T, X.device)
+        fq.fq_encode(ctx, X, T, nu, codes)
+        sums.zero_()
+        counts.zero_()
+        fq.fq_centroid_sums(ctx, X, T, nu, codes, sums, counts)
+        rows = float((nu > 0).sum().item())
+        ctx.close()
+        S, M = sums.cpu().numpy(), counts.cpu().numpy()
+        Cf = C.astype(np.float32).astype(np.float64)      # the codebook the device searched
+        mse = (rows - 2.0 * float(np.sum(S * Cf)) + float(np.sum(M * np.sum(Cf * Cf, axis=1)))) / (rows * (d // k))
+        return S, M, mse
+
+    S, M, mse = assign(C)
+    for _ in range(iters):
+        live = M > 0
+        C[live] = S[live] / M[live, None]
+        S, M, new = assign(C)
+        done = mse - new <= rtol * mse
+        mse = new
+        if done:
+            break
+    return C, mse
+
+
+def build_gpu(kind: str, d: int, k: int, N: int, train_rows, iters: int, restart_gaussians=(), s: float = 0.5,
+              device: int = 0) -> tuple[np.ndarray, float]:
+    """``build`` with the Lloyd iterations on the GPU (``refine_gpu``). train_rows: fp16 [T, d]
+    rows (any array; copied to the device)."""
+    import torch
+    X = torch.as_tensor(np.ascontiguousarray(train_rows, dtype=np.float16)).to(f"cuda:{device}")
+    C0 = initial(kind, d, k, N, s)
+    best = refine_gpu(C0, X, iters, device=device)
+    for G in restart_gaussians:
+        cand = refine_gpu(C0 @ haar(G).T, X, iters, device=device)
         if cand[1] < best[1]:
             best = cand
     return best

@@ -276,6 +276,20 @@ int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, co
     return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
 }
 
+int fq_centroid_sums(fq_ctx *ctx, const void *x, int64_t M, const float *nu, const uint32_t *codes,
+                     double *sums, double *counts, void *stream) {
+    if (!ctx || M < 0 || M > INT32_MAX) return FQ_EINVAL;
+    if (M == 0) return FQ_OK;
+    if (!x || !nu || !codes || !sums || !counts) return FQ_EINVAL;
+    if (fq_code_words(ctx, M) < 0) return FQ_EINVAL;
+    if (!aligned(x, 16) || !aligned(nu, 4) || !aligned(codes, 4) || !aligned(sums, 8) || !aligned(counts, 8))
+        return FQ_EALIGN;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    cudaError_t e = fq::launch_centroid_sums(ctx, (const __half *)x, M, nu, codes, sums, counts, (cudaStream_t)stream);
+    return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
 int fq_status(fq_ctx *ctx, void *stream, uint32_t *flags) {
     if (!ctx || !flags) return FQ_EINVAL;
     DeviceGuard g(ctx->device);

@@ -1,0 +1,69 @@
+"""Codebook Lloyd iterations on the GPU (assignment by the library's encoder, centroids by
+fq_centroid_sums) against the oracle's Lloyd iteration on the same training blocks."""
+import numpy as np
+import pytest
+
+from oracle import codebook as ocb
+from random_access_kv_gb300 import codebook as pcb
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import random_access_kv_gb300 as fq  # noqa: E402
+from random_access_kv_gb300 import build as fbuild  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    fbuild.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def blocks(X16, k):
+    """The training draws the GPU sees: every k-block of each fp16 row over the row's norm."""
+    X = X16.astype(np.float64)
+    U = X / np.linalg.norm(X, axis=1, keepdims=True)
+    return U.reshape(-1, k)
+
+
+@pytest.mark.parametrize("kind,d,k,N", [("spiral", 64, 2, 256), ("kronecker", 64, 4, 1024), ("kronecker", 128, 8, 512),
+                                        ("kronecker", 64, 1, 16), ("sphere", 64, 64, 256)], ids=lambda v: str(v))
+def test_one_lloyd_step_matches_the_oracle(kind, d, k, N):
+    r = np.random.default_rng([d, k, N])
+    X16 = r.standard_normal((3000 if k < d else 40000, d)).astype(np.float16)
+    C0 = ocb.initial_codebook(kind, d, k, N, 0.37 if k == d else 0.5)
+    # oracle: one Lloyd step on the same draws
+    C1_orc, hist = ocb.lloyd(C0, blocks(X16, k), iters=1, tol=0.0)
+    # GPU: one Lloyd step
+    C1_gpu, mse1 = pcb.refine_gpu(C0, torch.from_numpy(X16).cuda(), iters=1, rtol=0.0)
+    # Blocks whose nearest codewords tie within fp32 may land in either cell; away from those the
+    # centroids agree to fp32 accuracy of the block coordinates.
+    diff = np.abs(C1_gpu - C1_orc).max(axis=1)
+    assert np.mean(diff < 1e-5) > 0.99, diff.max()
+    assert mse1 == pytest.approx(hist[-1], rel=1e-4)
+
+
+def test_gpu_build_reaches_the_host_builders_distortion():
+    d, k, N = 64, 2, 64
+    r = np.random.default_rng(9)
+    X16 = r.standard_normal((40000, d)).astype(np.float16)
+    C_gpu, mse_gpu = pcb.build_gpu("spiral", d, k, N, X16, iters=15)
+    C_host, mse_host = pcb.build("spiral", d, k, N, r.standard_normal((40000 * d // k, d)), 15)
+    assert mse_gpu == pytest.approx(mse_host, rel=0.01)
+
+
+def test_centroid_sums_argument_checks():
+    C = ocb.spiral_codebook(64, 16).astype(np.float32)
+    ctx = fq.fq_codebook_load(C, np.eye(64, dtype=np.float32))
+    x = torch.zeros((10, 64), dtype=torch.float16, device="cuda")
+    nu, codes = fq.alloc_store(ctx, 10)
+    sums = torch.zeros((16, 2), dtype=torch.float64, device="cuda")
+    counts = torch.zeros(16, dtype=torch.float64, device="cuda")
+    fq.fq_centroid_sums(ctx, x, 0, nu, codes, sums, counts)        # no rows: no-op
+    with pytest.raises(fq.FQError):
+        fq.fq_centroid_sums(ctx, x, -1, nu, codes, sums, counts)
+    fq.fq_encode(ctx, x, 10, nu, codes)
+    fq.fq_centroid_sums(ctx, x, 10, nu, codes, sums, counts)       # zero rows are skipped
+    torch.cuda.synchronize()
+    assert float(counts.sum()) == 0.0 and float(sums.abs().sum()) == 0.0
+    ctx.close()

@@ -402,13 +402,27 @@ def run_ours(args) -> None:
     vec_per_step = MT + G
     value = world * vec_per_step * args.steps / (total_ms / 1e3)
 
-    # End to end through the public API from pinned host memory: H2D of the inputs, encode,
-    # decode, D2H of the codes, norms and decoded rows, every step.
+    # End to end through the public API from pinned host memory, every step: H2D of the inputs,
+    # encode, decode, D2H of the norms, codes and decoded rows. The step is cut into row chunks on
+    # three streams (copy in, compute, copy out), so that the copies overlap the kernels and each
+    # other; the events bracket all of it. Chunks start on whole 32-bit code words (1024-row
+    # multiples), so each chunk's records are its own words and a chunk is a store of its own.
     nu_host = torch.empty_like(nu, device="cpu").pin_memory()
     code_host = torch.empty_like(codes, device="cpu").pin_memory()
     out_host = torch.empty_like(out, device="cpu").pin_memory()
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    if streaming:
+        bounds = None
+    else:
+        # At least 16 MB of input per chunk: each chunk costs tens of microseconds of host-side
+        # issue (copies, events, a launch), which smaller chunks would not hide.
+        nch = max(1, min(8, (MT * d * 2) // (16 << 20)))
+        bounds = sorted({min(MT, (MT * c // nch) // 1024 * 1024) for c in range(nch)} | {MT})
 
-    def e2e_step():
+    def words(r):                                   # first code word of row r (r on a word boundary)
+        return (r * R + 31) // 32
+
+    def e2e_serial():
         xs.copy_(x_host, non_blocking=True)
         if gathers:
             idx.copy_(i_host, non_blocking=True)
@@ -416,6 +430,60 @@ def run_ours(args) -> None:
         nu_host.copy_(nu, non_blocking=True)
         code_host.copy_(codes, non_blocking=True)
         out_host.copy_(out, non_blocking=True)
+
+    def e2e_step():
+        if not streaming and len(bounds) == 2:    # one chunk: nothing to overlap
+            e2e_serial()
+            return
+        ev0 = torch.cuda.Event()
+        ev0.record(stream)
+        for st in (s_in, s_cmp, s_out):
+            st.wait_event(ev0)
+        if gathers:
+            with torch.cuda.stream(s_in):
+                idx.copy_(i_host, non_blocking=True)
+        if streaming:
+            for st in range(n_steps):
+                with torch.cuda.stream(s_in):
+                    xs[st].copy_(x_host[st], non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+                s_cmp.wait_event(e_in)
+                fq.fq_encode_append(ctx, xs[st], nt * n_seq, new, T, st * new, nu, codes, s_cmp.cuda_stream)
+        else:
+            for a, b in zip(bounds[:-1], bounds[1:]):
+                with torch.cuda.stream(s_in):
+                    xs[a:b].copy_(x_host[a:b], non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+                s_cmp.wait_event(e_in)
+                fq.fq_encode(ctx, xs[a:b], b - a, nu[a:], codes[words(a):], 0, s_cmp.cuda_stream)
+                if not gathers:
+                    fq.fq_decode(ctx, nu[a:], codes[words(a):], b - a, out[a:b], s_cmp.cuda_stream)
+                e_c = torch.cuda.Event()
+                e_c.record(s_cmp)
+                s_out.wait_event(e_c)
+                with torch.cuda.stream(s_out):
+                    nu_host[a:b].copy_(nu[a:b], non_blocking=True)
+                    code_host[words(a):words(b)].copy_(codes[words(a):words(b)], non_blocking=True)
+                    if not gathers:
+                        out_host[a:b].copy_(out[a:b], non_blocking=True)
+        if gathers:
+            e_idx = torch.cuda.Event()                # the index copy and every x chunk have landed
+            e_idx.record(s_in)
+            s_cmp.wait_event(e_idx)
+            fq.fq_decode_gather(ctx, nu, codes, MT, idx, G, out, s_cmp.cuda_stream)
+            e_c = torch.cuda.Event()
+            e_c.record(s_cmp)
+            s_out.wait_event(e_c)
+            with torch.cuda.stream(s_out):
+                if streaming:
+                    nu_host.copy_(nu, non_blocking=True)
+                    code_host.copy_(codes, non_blocking=True)
+                out_host.copy_(out, non_blocking=True)
+        e_end = torch.cuda.Event()
+        e_end.record(s_out)
+        stream.wait_event(e_end)
 
     for _ in range(3):
         e2e_step()

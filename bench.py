@@ -59,6 +59,22 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest x over all ranks (the job's time is its slowest rank's); x itself at N = 1."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank_step: int, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (max_total_ms / 1e3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -393,14 +409,11 @@ def run_ours(args) -> None:
     # Per-kernel times for the roofline, each launch timed on its own.
     enc_step_ms = timed_alone(encode_all, max(3, args.steps))
     dec_step_ms = timed_alone(decode_all, max(3, args.steps))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     flags = fq.fq_status(ctx, sp)
 
     vec_per_step = MT + G
-    value = world * vec_per_step * args.steps / (total_ms / 1e3)
+    value = job_value(vec_per_step, args.steps, world, total_ms)
 
     # End to end through the public API from pinned host memory, every step: H2D of the inputs,
     # encode, decode, D2H of the norms, codes and decoded rows. The step is cut into row chunks on
@@ -500,11 +513,8 @@ def run_ours(args) -> None:
     h2d = x_host.numel() * 2 + (i_host.numel() * 8 if gathers else 0)
     d2h = nu_host.numel() * 4 + code_host.numel() * 4 + out_host.numel() * 2
     e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * vec_per_step * args.steps / (e2e_total / 1e3)
+    e2e_total = max_over_ranks(e2e_total, world, dev)
+    e2e_value = job_value(vec_per_step, args.steps, world, e2e_total)
 
     enc_b, gat_b = workload_bytes(w, R)
     if not gathers:
@@ -660,12 +670,9 @@ def run_attend(args) -> None:
     clocks = sampler.stop()
     ms = [a.elapsed_time(b) for a, b in evs]
     total_ms = sum(ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     vec_per_step = 2 * groups * T
-    value = world * vec_per_step * args.steps / (total_ms / 1e3)
+    value = job_value(vec_per_step, args.steps, world, total_ms)
 
     # End to end: the cache stays resident (it is the KV cache); each step copies its queries in
     # from pinned host memory and the attention outputs back.
@@ -683,11 +690,8 @@ def run_attend(args) -> None:
         if i >= 3:
             e2e_ms.append(a.elapsed_time(b))
     e2e_total = sum(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * vec_per_step * args.steps / (e2e_total / 1e3)
+    e2e_total = max_over_ranks(e2e_total, world, dev)
+    e2e_value = job_value(vec_per_step, args.steps, world, e2e_total)
 
     # Fidelity: cosine with exact attention (fp64 on the device) over the uncompressed fp16 K and V,
     # and, as a full-size consistency check of the fused kernel, over the same cache decoded by

@@ -70,7 +70,8 @@ enum {
  * Derived tables built here, on the host in double precision: |c_n|^2, the rotated codebook
  * C Pi for k = d, and the split half-precision copies of Pi used by the tensor-core rotation.
  * Returns FQ_OK and *out, or an error and *out = NULL. The caller keeps ownership of the host
- * arrays. Blocking (copies complete before return).
+ * arrays. Blocking (copies complete before return). With FQ_TEST_FAIL_ALLOC set in the
+ * environment its device allocations fail, so that the FQ_ENOMEM path can be tested.
  */
 int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k,
                      const float *Pi_host, int d, int device);
@@ -163,6 +164,14 @@ int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, co
  */
 int fq_centroid_sums(fq_ctx *ctx, const void *x, int64_t M, const float *nu, const uint32_t *codes,
                      double *sums, double *counts, void *stream);
+
+/*
+ * fq_selftest_wait - exercise the failure path of the kernels' bounded waits: a kernel waits on
+ * a barrier that nothing completes, gives up after about limit_ns nanoseconds (at most 1e9) and
+ * sets FQ_FLAG_TIMEOUT, which the next fq_status reports. Nothing traps; the context stays usable.
+ * (The codec itself has no counterpart; the method's pages describe no failure handling.)
+ */
+int fq_selftest_wait(fq_ctx *ctx, uint64_t limit_ns, void *stream);
 
 /* Number of uint32 words of a store of M records: ceil(M R / 32). Returns -1 on bad arguments. */
 int64_t fq_code_words(const fq_ctx *ctx, int64_t M);

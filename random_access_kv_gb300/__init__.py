@@ -10,7 +10,7 @@ All device buffers are torch CUDA tensors owned by the caller; ``alloc_store`` s
 from ._binding import (  # noqa: F401
     FQ_FLAG_NONFINITE, FQ_FLAG_RANGE, FQ_FLAG_TIMEOUT, Context, FQError, FQLibraryMissing,
     fq_attend, fq_centroid_sums, fq_code_words, fq_codebook_load, fq_decode, fq_decode_gather, fq_decode_gather_f32, fq_destroy,
-    fq_encode, fq_encode_append, fq_record_bits, fq_shape, fq_status, fq_strerror, header_symbols,
+    fq_encode, fq_encode_append, fq_record_bits, fq_selftest_wait, fq_shape, fq_status, fq_strerror, header_symbols,
 )
 
 

@@ -43,6 +43,7 @@ _SIGNATURES = {
     "fq_attend": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p, _i64, _i64, _i64, _i64, _i64, _i64,
                          ctypes.c_float, _c_void_p, _c_void_p]),
     "fq_centroid_sums": (_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "fq_selftest_wait": (_int, [_c_void_p, ctypes.c_uint64, _c_void_p]),
     "fq_code_words": (_i64, [_c_void_p, _i64]),
     "fq_record_bits": (_int, [_c_void_p]),
     "fq_shape": (_int, [_c_void_p, ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
@@ -179,6 +180,10 @@ def fq_attend(ctx: Context, nu, codes, M: int, q, n_queries: int, q_per_group: i
 def fq_centroid_sums(ctx: Context, x, M: int, nu, codes, sums, counts, stream=None) -> None:
     _check("fq_centroid_sums", lib().fq_centroid_sums(ctx, _ptr(x), int(M), _ptr(nu), _ptr(codes), _ptr(sums),
                                                       _ptr(counts), _stream(stream)))
+
+
+def fq_selftest_wait(ctx: Context, limit_ns: int, stream=None) -> None:
+    _check("fq_selftest_wait", lib().fq_selftest_wait(ctx, int(limit_ns), _stream(stream)))
 
 
 def fq_code_words(ctx: Context, M: int) -> int:

@@ -25,6 +25,9 @@ This is construction-time code, not part of the encode/decode path.
 """
 from __future__ import annotations
 
+import struct
+import zlib
+
 import numpy as np
 from scipy import special
 
@@ -228,3 +231,48 @@ def for_workload(cfg: int) -> tuple[np.ndarray, np.ndarray]:
                  w.lloyd_iters, [synth.restart_gaussian(cfg, w.k, r) for r in range(1, w.lloyd_restarts)],
                  synth.kronecker_offset(cfg))
     return C.astype(np.float32), Pi
+
+
+# Codebook file (.fqb): the persistent state of a codec, i.e. the shared codebook and rotation with
+# how they were built. Little-endian: a header, then C float32 [N x k] and Pi float32 [d x d] (row
+# major), then the CRC-32 of everything before it.
+FQB_MAGIC = b"FQB1"
+FQB_VERSION = 1
+_FQB_HEADER = struct.Struct("<4sIIII16sqIIQd")   # magic, version, d, k, N, kind, seed, iters, restarts, draws, mse
+
+
+def save_fqb(path: str, C: np.ndarray, Pi: np.ndarray, kind: str, seed: int = 0, iters: int = 0,
+             restarts: int = 0, draws: int = 0, mse: float = float("nan")) -> None:
+    C = np.ascontiguousarray(C, dtype="<f4")
+    Pi = np.ascontiguousarray(Pi, dtype="<f4")
+    N, k = C.shape
+    d = Pi.shape[0]
+    if Pi.shape != (d, d):
+        raise ValueError("Pi must be square")
+    head = _FQB_HEADER.pack(FQB_MAGIC, FQB_VERSION, d, k, N, kind.encode()[:16].ljust(16, b"\0"), seed, iters,
+                            restarts, draws, mse)
+    body = head + C.tobytes() + Pi.tobytes()
+    with open(path, "wb") as f:
+        f.write(body + struct.pack("<I", zlib.crc32(body)))
+
+
+def load_fqb(path: str) -> tuple[np.ndarray, np.ndarray, dict]:
+    """(C float32 [N, k], Pi float32 [d, d], metadata). Raises ValueError on a damaged file."""
+    with open(path, "rb") as f:
+        data = f.read()
+    if len(data) < _FQB_HEADER.size + 4:
+        raise ValueError("fqb: truncated header")
+    magic, version, d, k, N, kind, seed, iters, restarts, draws, mse = _FQB_HEADER.unpack_from(data)
+    if magic != FQB_MAGIC or version != FQB_VERSION:
+        raise ValueError("fqb: not a codebook file of this version")
+    size = _FQB_HEADER.size + 4 * (N * k + d * d)
+    if len(data) != size + 4:
+        raise ValueError("fqb: size does not match the header")
+    if struct.unpack_from("<I", data, size)[0] != zlib.crc32(data[:size]):
+        raise ValueError("fqb: CRC mismatch")
+    o = _FQB_HEADER.size
+    C = np.frombuffer(data, dtype="<f4", count=N * k, offset=o).reshape(N, k).astype(np.float32)
+    Pi = np.frombuffer(data, dtype="<f4", count=d * d, offset=o + 4 * N * k).reshape(d, d).astype(np.float32)
+    meta = {"d": d, "k": k, "N": N, "kind": kind.rstrip(b"\0").decode(), "seed": seed, "lloyd_iters": iters,
+            "restarts": restarts, "draws": draws, "mse": mse}
+    return C, Pi, meta

@@ -53,8 +53,13 @@ void free_ctx(fq_ctx *c) {
     free(c);
 }
 
+// FQ_TEST_FAIL_ALLOC set in the environment: device allocations of fq_codebook_load fail, to test
+// the out-of-memory path (the context is released and FQ_ENOMEM returned).
+bool fail_alloc() { return getenv("FQ_TEST_FAIL_ALLOC") != nullptr; }
+
 template <typename T>
 cudaError_t upload(T **dst, const std::vector<T> &src) {
+    if (fail_alloc()) return cudaErrorMemoryAllocation;
     cudaError_t e = cudaMalloc((void **)dst, src.size() * sizeof(T));
     if (e != cudaSuccess) return e;
     return cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice);
@@ -288,6 +293,13 @@ int fq_centroid_sums(fq_ctx *ctx, const void *x, int64_t M, const float *nu, con
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaError_t e = fq::launch_centroid_sums(ctx, (const __half *)x, M, nu, codes, sums, counts, (cudaStream_t)stream);
     return e == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
+int fq_selftest_wait(fq_ctx *ctx, uint64_t limit_ns, void *stream) {
+    if (!ctx || limit_ns > 1000000000ull) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    return fq::launch_wait_selftest(ctx, limit_ns, (cudaStream_t)stream) == cudaSuccess ? FQ_OK : FQ_ECUDA;
 }
 
 int fq_status(fq_ctx *ctx, void *stream, uint32_t *flags) {

@@ -88,6 +88,7 @@ cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, R
                                 uint32_t *codes, cudaStream_t s);
 cudaError_t launch_centroid_sums(const fq_ctx *ctx, const __half *x, int64_t M, const float *nu,
                                  const uint32_t *codes, double *sums, double *counts, cudaStream_t s);
+cudaError_t launch_wait_selftest(const fq_ctx *ctx, uint64_t limit_ns, cudaStream_t s);
 cudaError_t prepare_attend(fq_ctx *ctx);
 cudaError_t launch_attend(const fq_ctx *ctx, const float *nu, const uint32_t *codes, const __half *q,
                           int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,

@@ -50,7 +50,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "KV vectors/s encoded and decoded (fp16 GB/s) per bitrate; % of HBM/TC roofline"
-ATTEND_METRIC = "cached KV vectors/s attended (fused decode-into-attention, one query per head)"
+ATTEND_METRIC = "cached KV vectors/s attended (fused decode-into-attention)"
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -628,6 +628,8 @@ def run_attend(args) -> None:
     if args.groups:
         groups = min(groups, args.groups)
     M, d = groups * T, w.d
+    qpg = args.q_per_group
+    nq = groups * qpg
     scale = 1.0 / float(np.sqrt(d))
     # The cache: K rows [0, M), V rows [M, 2M) of one store, encoded once (untimed).
     nu, codes = fq.alloc_store(ctx, 2 * M, dev)
@@ -636,15 +638,15 @@ def run_attend(args) -> None:
         fq.fq_encode(ctx, x, M, nu, codes, t * M)
         del x
     torch.cuda.synchronize(dev)
-    q_host = torch.from_numpy(synth.query_rows(cfg, groups, d)).pin_memory()
+    q_host = torch.from_numpy(synth.query_rows(cfg, nq, d)).pin_memory()
     q = q_host.to(dev)
-    out = torch.empty((groups, d), dtype=torch.float32, device=dev)
+    out = torch.empty((nq, d), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
     def step():
-        fq.fq_attend(ctx, nu, codes, 2 * M, q, groups, 1, T, 0, M, T, scale, out, sp)
+        fq.fq_attend(ctx, nu, codes, 2 * M, q, nq, qpg, T, 0, M, T, scale, out, sp)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -702,24 +704,24 @@ def run_attend(args) -> None:
     cos, cos_dec = [], []
     k_all, v_all = synth.kv_tensor(cfg, 0, rows=M), synth.kv_tensor(cfg, 1, rows=M)
 
-    def attention(Kx, Vx, qx):
-        p = torch.softmax(scale * torch.einsum("gtd,gd->gt", Kx, qx), dim=1)
-        return torch.einsum("gt,gtd->gd", p, Vx)
+    def attention(Kx, Vx, qx):             # qx [groups, qpg, d]
+        p = torch.softmax(scale * torch.einsum("gtd,gqd->gqt", Kx, qx), dim=2)
+        return torch.einsum("gqt,gtd->gqd", p, Vx).reshape(-1, d)
 
     for g0 in range(0, groups, 64):
         g1 = min(groups, g0 + 64)
         n = (g1 - g0) * T
         Kx = torch.from_numpy(k_all[g0 * T:g1 * T]).to(dev).double().view(g1 - g0, T, d)
         Vx = torch.from_numpy(v_all[g0 * T:g1 * T]).to(dev).double().view(g1 - g0, T, d)
-        cos.append(torch.nn.functional.cosine_similarity(attention(Kx, Vx, q[g0:g1].double()),
-                                                         o_fused[g0:g1], dim=1).cpu())
+        qg = q[g0 * qpg:g1 * qpg].double().view(g1 - g0, qpg, d)
+        og = o_fused[g0 * qpg:g1 * qpg]
+        cos.append(torch.nn.functional.cosine_similarity(attention(Kx, Vx, qg), og, dim=1).cpu())
         del Kx, Vx
         rows = torch.arange(g0 * T, g1 * T, device=dev)
         dec = torch.empty((2 * n, d), dtype=torch.float32, device=dev)
         fq.fq_decode_gather_f32(ctx, nu, codes, 2 * M, torch.cat([rows, rows + M]), 2 * n, dec, sp)
         dec = dec.double().view(2, g1 - g0, T, d)
-        cos_dec.append(torch.nn.functional.cosine_similarity(attention(dec[0], dec[1], q[g0:g1].double()),
-                                                             o_fused[g0:g1], dim=1).cpu())
+        cos_dec.append(torch.nn.functional.cosine_similarity(attention(dec[0], dec[1], qg), og, dim=1).cpu())
         del dec
     del k_all, v_all
     cos = torch.cat(cos).numpy()
@@ -727,7 +729,7 @@ def run_attend(args) -> None:
     flags = fq.fq_status(ctx, sp)
 
     launch_ms = statistics.mean(ms)
-    alg_bytes = groups * T * 2 * (R / 8 + 4) + groups * d * (2 + 4)
+    alg_bytes = groups * T * 2 * (R / 8 + 4) + nq * d * (2 + 4)
     peaks = measured_peaks()
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     roofline = {"kernel": "attend", "cuda_kernel": "attend", "traffic": committed_traffic("attend", cfg, groups * T),
@@ -743,11 +745,12 @@ def run_attend(args) -> None:
     if rank == 0:
         line = {
             "metric": ATTEND_METRIC, "value": value, "unit": "vectors/s", "n_gpus": world, "steps": args.steps,
+            "query_token_pairs_per_s": world * nq * T * args.steps / (total_ms / 1e3),
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name + " -- fused attention"
                        + (f" (first {groups} groups)" if groups * T != w.rows else ""), "groups": groups, "tokens_per_group": T,
-                       "queries_per_group": 1, "d": d, "k": w.k, "N": w.N, "record_bits": R,
+                       "queries_per_group": qpg, "d": d, "k": w.k, "N": w.N, "record_bits": R,
                        "layout": "K rows [0, M), V rows [M, 2M) of one code store; one launch per step",
                        "l2": "flushed before every timed step (256 MB write, outside the step events)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -923,6 +926,8 @@ def main():
                     help="relative MSE and throughput against bits per coordinate (scalar k = 1 vs FibQuant)")
     ap.add_argument("--lloyd", action="store_true",
                     help="codebook building: host numpy Lloyd against the GPU Lloyd for --workload")
+    ap.add_argument("--q-per-group", type=int, default=1,
+                    help="with --attend: queries per cached (layer, head) group (grouped-query attention)")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --attend: the first G (layer, head) groups only (a small case for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -273,7 +273,7 @@ int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, co
         if (groups > 1 && stride > (M - T - r0) / (groups - 1)) return FQ_EINVAL;
     }
     if (!aligned(nu, 4) || !aligned(codes, 4) || !aligned(q, 2) || !aligned(out, 4)) return FQ_EALIGN;
-    if (!ctx->attend_nwarps) return FQ_EINVAL;
+    if (!fq::attend_supported(ctx)) return FQ_EINVAL;
     DeviceGuard g(ctx->device);
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaError_t e = fq::launch_attend(ctx, nu, codes, (const __half *)q, n_queries, q_per_group, T, k_row0,

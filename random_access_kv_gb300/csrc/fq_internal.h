@@ -33,14 +33,19 @@ struct fq_ctx {
     // k = 4, 8 tensor-core encoder table
     uint8_t *cb_ops;             // codebook rows as MMA B operands (see fq_encode_kq.cu)
     int kq_max_ctas;
-    // fused attention launch shape (attend_nwarps == 0: the configuration does not fit)
     int smem_optin;              // dynamic shared memory a CTA may opt in to
-    int attend_lut, attend_nwarps, attend_max_split;
-    int64_t attend_slots[9];     // co-resident CTAs of the fused attention kernel per cluster size
-    size_t attend_smem;
+    // fused attention launch plans: [0] one query per cluster, [1] four queries of one group
+    // (nwarps == 0: the plan does not fit)
+    struct AttendPlan {
+        int qg, lut, nwarps, max_split;
+        int64_t slots[9];        // co-resident CTAs per cluster size
+        size_t smem;
+    } attend[2];
 };
 
 namespace fq {
+
+using AttendPlan = fq_ctx::AttendPlan;
 
 // Mapping from an input row r to its store row: (r / n_new) * seq_cap + row_base + r % n_new.
 // fq_encode uses n_new = M (one sequence) and row_base = row0.
@@ -93,7 +98,7 @@ cudaError_t prepare_attend(fq_ctx *ctx);
 cudaError_t launch_attend(const fq_ctx *ctx, const float *nu, const uint32_t *codes, const __half *q,
                           int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,
                           int64_t stride, float scale, float *out, cudaStream_t s);
-int attend_split(const fq_ctx *ctx, int64_t n_queries, int64_t T);
+bool attend_supported(const fq_ctx *ctx);
 // One-time kernel attribute set-up (dynamic shared memory limits); called by fq_codebook_load.
 cudaError_t prepare_encode_blocks(const fq_ctx *ctx);
 cudaError_t prepare_decode_blocks(const fq_ctx *ctx);

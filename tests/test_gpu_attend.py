@@ -90,9 +90,20 @@ def test_attend_interleaved_long_split(shape):
     run_case(shape, 2, T, 0, T, 2 * T, sub=1)
 
 
-@pytest.mark.parametrize("shape", [SHAPES[1], SHAPES[3], SHAPES[5]], ids=lambda s: f"d{s[0]}k{s[1]}")
-def test_attend_several_queries_per_group(shape):
-    run_case(shape, 3, 130, 0, 3 * 130, 130, qpg=4, sub=2)
+@pytest.mark.parametrize("shape", [SHAPES[1], SHAPES[2], SHAPES[3], SHAPES[4], SHAPES[5], SHAPES[8]],
+                         ids=lambda s: f"d{s[0]}k{s[1]}N{s[2]}")
+@pytest.mark.parametrize("qpg", [2, 4, 8])
+def test_attend_several_queries_per_group(shape, qpg):
+    # q_per_group a multiple of 4: clusters serve four queries of a group together, sharing the
+    # decode; otherwise one query per cluster
+    run_case(shape, 3, 130, 0, 3 * 130, 130, qpg=qpg, sub=2)
+
+
+@pytest.mark.parametrize("shape", [SHAPES[1], SHAPES[3]], ids=lambda s: f"d{s[0]}k{s[1]}")
+def test_attend_grouped_queries_long_split(shape):
+    # four queries per group over 5000 tokens: grouped clusters split over several CTAs
+    T = 5000
+    run_case(shape, 2, T, 0, T, 2 * T, qpg=4, sub=4)
 
 
 @pytest.mark.parametrize("shape", [SHAPES[1], SHAPES[4]], ids=lambda s: f"d{s[0]}k{s[1]}")

@@ -94,9 +94,9 @@ def measured_peaks() -> dict:
 
 # The source file of each timed kernel; its hash (with the shared headers) ties a committed ncu
 # traffic figure to the code it measured.
-KERNEL_SOURCES = {"encode_k2_tc": "fq_encode_k2.cu", "encode_kq_tc": "fq_encode_kq.cu",
-                  "encode_full_tc": "fq_encode_full_tc.cu", "decode_tc": "fq_decode_tc.cu",
-                  "decode_full_simple": "fq_full.cu", "attend": "fq_attend.cu"}
+KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu"],
+                  "encode_full_tc": ["fq_encode_full_tc.cu"], "decode_tc": ["fq_decode_tc.cu"],
+                  "decode_full_simple": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"]}
 
 
 def source_hash(kernel: str) -> str:
@@ -104,7 +104,7 @@ def source_hash(kernel: str) -> str:
     cdir = os.path.join(ROOT, "random_access_kv_gb300", "csrc")
     # The kernel's file and the device-code headers it includes (fq_internal.h holds host-side
     # declarations and the context struct, which change without changing any kernel).
-    for name in [KERNEL_SOURCES[kernel], "fq_sm100.cuh", "fq_bits.cuh"]:
+    for name in KERNEL_SOURCES[kernel] + ["fq_sm100.cuh", "fq_bits.cuh"]:
         with open(os.path.join(cdir, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

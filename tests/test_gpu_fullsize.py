@@ -118,3 +118,34 @@ def test_streaming_append_long_context():
                         nu_d[torch.from_numpy(rows).cuda()].cpu().numpy(), idx, C, Pi, fp16_output=True)
     assert fq.fq_status(ctx) == 0
     ctx.close()
+
+
+@pytest.mark.parametrize("cfg,qpg", [(2, 1), (4, 1), (4, 4)])
+def test_attend_full_size_sampled_groups(cfg, qpg):
+    """Fused attention at the workload's full size, in the benchmark's launch configuration (keys at
+    rows [0, M), values at [M, 2M), one group per (layer, head)), over a random store; sampled
+    groups checked against the oracle's fp64 attention over the decoded records."""
+    from oracle import attention  # noqa: F401  (the oracle module the check uses)
+    w = synth.WORKLOADS[cfg]
+    C, Pi = ow.codebook(cfg), ow.rotation(cfg)
+    ctx = fq.fq_codebook_load(C, Pi)
+    T = int(w.shape[-2])
+    groups = w.rows // T
+    M = w.rows
+    nb, B = w.d // w.k, w.B
+    nu, words = synth.random_store(cfg, 2 * M, fq.fq_code_words(ctx, 2 * M), sub=7)
+    q = synth.query_rows(cfg, groups * qpg, w.d, sub=7)
+    scale = 1.0 / np.sqrt(w.d)
+    out = torch.empty((groups * qpg, w.d), dtype=torch.float32, device="cuda")
+    fq.fq_attend(ctx, torch.from_numpy(nu).cuda(), torch.from_numpy(words.view(np.int32)).cuda(), 2 * M,
+                 torch.from_numpy(q).cuda(), groups * qpg, qpg, T, 0, M, T, scale, out)
+    torch.cuda.synchronize()
+    assert fq.fq_status(ctx) == 0
+    got = out.cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for g in sorted({0, groups - 1} | set(synth.gather_indices(cfg, 9, groups, 2, replace=False).tolist())):
+        kr, vr = g * T, M + g * T
+        parity.check_attention(got[g * qpg:(g + 1) * qpg], q[g * qpg:(g + 1) * qpg].astype(np.float64),
+                               nu[kr:kr + T], ofq.record_range(words, kr, T, nb, B),
+                               nu[vr:vr + T], ofq.record_range(words, vr, T, nb, B), C, Pi, scale)
+    ctx.close()

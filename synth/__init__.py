@@ -64,8 +64,8 @@ class Workload:
         return int(round(math.log2(self.N)))
 
 
-# The five workloads. Lloyd budgets other than workload 1's five iterations are this build's
-# choice (the pages fix none): they bound codebook-building time on the host.
+# The five workloads. Lloyd budgets other than workload 1's five iterations are chosen here (the
+# pages fix none): they bound codebook-building time on the host.
 WORKLOADS = {
     1: Workload(1, "tiny: 4096x64 N(0,1), k=2 N=16 (b=2)", (4096, 64), 1, 2, 16, "gauss", "spiral",
                 4096, 5, 1, "encode+decode"),

@@ -96,7 +96,7 @@ def measured_peaks() -> dict:
 # traffic figure to the code it measured.
 KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu"],
                   "encode_full_tc": ["fq_encode_full_tc.cu"], "decode_tc": ["fq_decode_tc.cu"],
-                  "decode_full_simple": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"]}
+                  "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"]}
 
 
 def source_hash(kernel: str) -> str:
@@ -114,7 +114,7 @@ def kernel_of(w, op: str) -> str:
     """Name of the kernel that runs `op` ("encode" or "decode") for workload w."""
     if op == "encode":
         return "encode_full_tc" if w.k == w.d else ("encode_k2_tc" if w.k == 2 else "encode_kq_tc")
-    return "decode_full_simple" if w.k == w.d else "decode_tc"
+    return "decode_full" if w.k == w.d else "decode_tc"
 
 
 def committed_traffic(kernel: str, workload: int, rows_per_launch: int):

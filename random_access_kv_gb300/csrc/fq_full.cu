@@ -81,43 +81,44 @@ encode_full_simple(const __half *__restrict__ x, int64_t M, RowMap map,
     wr.flush();
 }
 
-template <int D, typename OutT>
+// x_hat = nu C_rot[i] for k = d. One warp per 32 output rows: each lane reads its row's index and
+// norm, then the warp writes the rows one after another, lane l covering columns 2l and 2l + 1, so
+// that every table read (256 B) and every row store (128 B fp16) is a single coalesced access.
+template <typename OutT>
 __global__ void __launch_bounds__(kThreads)
-decode_full_simple(const float *__restrict__ nu, const uint32_t *__restrict__ codes, int64_t M,
-                   const int64_t *__restrict__ idx, int64_t n, const float *__restrict__ Crot,
-                   int B, OutT *__restrict__ out, uint32_t *__restrict__ flags) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= n) return;
-    const int64_t row = idx ? __ldg(idx + j) : j;
-    float s = 0.f;
-    uint32_t i = 0;
-    if (row < 0 || row >= M) {
-        atomicOr(flags, (uint32_t)FQ_FLAG_RANGE);
-    } else {
-        BitReader rd(codes, row * (int64_t)B);
-        i = rd.get(B);
-        s = __ldg(nu + row);
-    }
-    const float4 *src = reinterpret_cast<const float4 *>(Crot + (size_t)i * D);
-    if constexpr (sizeof(OutT) == 2) {
-        uint4 *dst = reinterpret_cast<uint4 *>(out + j * D);
-#pragma unroll
-        for (int q = 0; q < D / 8; ++q) {
-            float4 a = __ldg(src + 2 * q), b = __ldg(src + 2 * q + 1);
-            uint4 w;
-            __half2 *h = reinterpret_cast<__half2 *>(&w);
-            h[0] = __floats2half2_rn(a.x * s, a.y * s);
-            h[1] = __floats2half2_rn(a.z * s, a.w * s);
-            h[2] = __floats2half2_rn(b.x * s, b.y * s);
-            h[3] = __floats2half2_rn(b.z * s, b.w * s);
-            dst[q] = w;
+decode_full(const float *__restrict__ nu, const uint32_t *__restrict__ codes, int64_t M,
+            const int64_t *__restrict__ idx, int64_t n, const float *__restrict__ Crot, int B,
+            OutT *__restrict__ out, uint32_t *__restrict__ flags) {
+    constexpr int D = 64;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t tile = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32; tile * 32 < n; tile += nwarps) {
+        const int64_t j = tile * 32 + lane;
+        float s = 0.f;
+        uint32_t i = 0;
+        if (j < n) {
+            const int64_t row = idx ? __ldg(idx + j) : j;
+            if (row < 0 || row >= M) {
+                atomicOr(flags, (uint32_t)FQ_FLAG_RANGE);
+            } else {
+                BitReader rd(codes, row * (int64_t)B);
+                i = rd.get(B);
+                s = __ldg(nu + row);
+            }
         }
-    } else {
-        float4 *dst = reinterpret_cast<float4 *>(out + j * D);
-#pragma unroll
-        for (int q = 0; q < D / 4; ++q) {
-            float4 a = __ldg(src + q);
-            dst[q] = make_float4(a.x * s, a.y * s, a.z * s, a.w * s);
+        const int rows = n - tile * 32 < 32 ? (int)(n - tile * 32) : 32;
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) {
+            const uint32_t ir = __shfl_sync(0xffffffffu, i, r);
+            const float sr = __shfl_sync(0xffffffffu, s, r);
+            if (r < rows) {
+                const float2 c = __ldg(reinterpret_cast<const float2 *>(Crot + (size_t)ir * D) + lane);
+                OutT *dst = out + (tile * 32 + r) * D;
+                if constexpr (sizeof(OutT) == 2)
+                    reinterpret_cast<__half2 *>(dst)[lane] = __floats2half2_rn(c.x * sr, c.y * sr);
+                else
+                    reinterpret_cast<float2 *>(dst)[lane] = make_float2(c.x * sr, c.y * sr);
+            }
         }
     }
 }
@@ -137,13 +138,14 @@ cudaError_t launch_decode_full(const fq_ctx *ctx, const float *nu, const uint32_
                                int64_t M, const int64_t *idx, int64_t n, void *out,
                                bool out_f32, cudaStream_t s) {
     if (ctx->d != 64) return cudaErrorInvalidValue;
-    const int64_t grid = (n + kThreads - 1) / kThreads;
+    int64_t grid = ((n + 31) / 32 + kThreads / 32 - 1) / (kThreads / 32);
+    if (grid > 8 * (int64_t)ctx->num_sms) grid = 8 * (int64_t)ctx->num_sms;
     if (out_f32)
-        decode_full_simple<64, float><<<(unsigned)grid, kThreads, 0, s>>>(nu, codes, M, idx, n, ctx->Crot,
-                                                                          ctx->B, (float *)out, ctx->flags);
+        decode_full<float><<<(unsigned)grid, kThreads, 0, s>>>(nu, codes, M, idx, n, ctx->Crot, ctx->B, (float *)out,
+                                                               ctx->flags);
     else
-        decode_full_simple<64, __half><<<(unsigned)grid, kThreads, 0, s>>>(nu, codes, M, idx, n, ctx->Crot,
-                                                                           ctx->B, (__half *)out, ctx->flags);
+        decode_full<__half><<<(unsigned)grid, kThreads, 0, s>>>(nu, codes, M, idx, n, ctx->Crot, ctx->B,
+                                                                (__half *)out, ctx->flags);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,11 @@ def test_strerror_and_null_context(L):
     assert L.fq_encode(None, None, 5, None, None, 0, None) == fb.FQ_EINVAL
     assert L.fq_decode_gather(None, None, None, 5, None, 5, None, None) == fb.FQ_EINVAL
     assert L.fq_shape(None, None, None, None) == fb.FQ_EINVAL
+    assert L.fq_attend(None, None, None, 10, None, 1, 1, 5, 0, 5, 5, 0.1, None, None) == fb.FQ_EINVAL
+    assert L.fq_centroid_sums(None, None, 10, None, None, None, None, None) == fb.FQ_EINVAL
+    assert L.fq_selftest_wait(None, 1000, None) == fb.FQ_EINVAL
+    assert L.fq_encode_append(None, None, 1, 1, 4, 0, None, None, None) == fb.FQ_EINVAL
+    assert L.fq_decode(None, None, None, 4, None, None) == fb.FQ_EINVAL
     L.fq_destroy(None)
 
 

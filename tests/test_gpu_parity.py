@@ -160,7 +160,8 @@ def _small_codebook(d, k, N, seed):
 
 @pytest.mark.parametrize("d,k,N", [(64, 4, 8), (64, 8, 2), (64, 2, 2), (128, 1, 8), (64, 64, 128),
                                    (128, 4, 64), (64, 1, 16), (64, 4, 256), (128, 8, 128), (64, 8, 512),
-                                   (128, 4, 1024), (128, 2, 64), (64, 2, 128), (64, 1, 2), (128, 1, 4)])
+                                   (128, 4, 1024), (128, 2, 64), (64, 2, 128), (64, 1, 2), (128, 1, 4),
+                                   (128, 2, 256), (64, 8, 4096), (128, 8, 4096)])
 @pytest.mark.parametrize("row0", [0, 1, 7, 45])
 def test_records_at_any_bit_offset_preserve_neighbours(d, k, N, row0):
     C, Pi = _small_codebook(d, k, N, d * 1000 + k * 10 + N)

@@ -307,8 +307,8 @@ def run_ours(args) -> None:
     if w.op not in ("encode+gather", "encode+decode", "stream+gather"):
         raise SystemExit(f"workload {cfg} ({w.op}) is not timed by bench.py")
     streaming = w.op == "stream+gather"
-    if streaming and args.rows:
-        raise SystemExit("--rows does not apply to the streaming workload")
+    if streaming and args.rows and args.rows % w.shape[-2]:
+        raise SystemExit(f"--rows must be a multiple of the sequence length {w.shape[-2]} here")
     gathers = w.op != "encode+decode"            # encode+decode workloads decode every row
     C, Pi = pcb.for_workload(cfg)
     ctx = fq.fq_codebook_load(C, Pi, local)
@@ -327,7 +327,7 @@ def run_ours(args) -> None:
 
         def arrival_order(a):  # [n_seq*T, d] -> [steps, n_seq, new, d], the order tokens arrive in
             return np.ascontiguousarray(a.reshape(n_seq, n_steps, new, d).transpose(1, 0, 2, 3))
-        x_np = np.concatenate([arrival_order(synth.kv_tensor(cfg, t)) for t in range(nt)], axis=1)
+        x_np = np.concatenate([arrival_order(synth.kv_tensor(cfg, t, rows=M)) for t in range(nt)], axis=1)
         x_np = x_np.reshape(n_steps, nt * n_seq * new, d)
     else:
         x_np = np.concatenate([synth.kv_tensor(cfg, t, rows=M) for t in range(nt)])

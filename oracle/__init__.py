@@ -18,4 +18,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle_*.py``):
   codebook.companded_radii     pinned (k = 2 closed form against scipy betaincinv)
   codebook.spiral / kronecker  pinned (golden angle, Roberts constants as polynomial roots)
   codebook.lloyd               pinned (MSE non-increasing, MSE falls with N, beats scalar Lloyd-Max)
+  fractal.vertices / encode    pinned (polygon closed forms, 40-digit unrolled recurrence)
+  fractal.decode / access      pinned (exhaustive round trips, adversarial strings at the segment
+                               limit, failure beyond it); fractal.append pinned against encode
+
+The iterated-map archive (``fractal``) follows a second page, "Fractal KV-Cache Archives"
+(gist.science summary of arXiv 2607.07144), cited there as [Archive §x].
 """

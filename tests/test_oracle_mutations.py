@@ -86,3 +86,55 @@ def test_shifted_radius_quantile_is_caught(monkeypatch):
 def test_wrong_source_law_is_caught(monkeypatch):
     monkeypatch.setattr(ocb, "source_points", lambda g, k: np.asarray(g)[:, :k] / np.sqrt(np.asarray(g).shape[1]))
     assert _fails(tc.test_source_points_law)
+
+
+# Iterated-map archive ("Fractal KV-Cache Archives", Method 1)
+
+import test_oracle_fractal as tf
+from oracle import fractal as ofa
+
+
+def test_swapped_contraction_weights_are_caught(monkeypatch):
+    # p_k = p_{k-1} + r (V - p_{k-1}) puts weight r on the vertex instead of 1 - r
+    def bad(symbols, N, r, start=(0.0, 0.0), V=None):
+        V = ofa.vertices(N) if V is None else V
+        x, y = start
+        for c in symbols:
+            x, y = x + r * (V[c, 0] - x), y + r * (V[c, 1] - y)
+        return float(x), float(y)
+    monkeypatch.setattr(ofa, "encode_segment", bad)
+    assert _fails(tf.test_encode_matches_unrolled_recurrence_to_40_digits, 16, 0.75, 9)
+
+
+def test_clockwise_polygon_is_caught(monkeypatch):
+    orig = ofa.vertices
+    monkeypatch.setattr(ofa, "vertices", lambda N: orig(N) * np.array([1.0, -1.0]))
+    assert _fails(tf.test_vertices_regular_polygon)
+    assert _fails(tf.test_encode_matches_unrolled_recurrence_to_40_digits, 16, 0.75, 9)
+
+
+def test_start_at_a_vertex_is_caught(monkeypatch):
+    orig = ofa.encode_segment
+    monkeypatch.setattr(ofa, "encode_segment",
+                        lambda s, N, r, start=(0.0, 0.0), V=None: orig(s, N, r, start=(1.0, 0.0), V=V))
+    assert _fails(tf.test_encode_matches_unrolled_recurrence_to_40_digits, 3, 0.5, 12)
+
+
+def test_inverse_without_vertex_term_is_caught(monkeypatch):
+    def bad(anchor, length, N, r, stop=0, V=None):
+        x, y = anchor
+        out = []
+        for _ in range(length - 1, stop - 1, -1):
+            c = ofa.nearest_cell(x, y, N, r)
+            out.append(c)
+            x, y = x / r, y / r
+        return out[::-1]
+    monkeypatch.setattr(ofa, "decode_segment", bad)
+    assert _fails(tf.test_round_trip_every_string, 3, 9)
+
+
+def test_optimistic_segment_bound_is_caught(monkeypatch):
+    # a bound that ignores the amplification allows segments too long to decode
+    orig = ofa.max_segment
+    monkeypatch.setattr(ofa, "max_segment", lambda N, r, cap=64: 3 * orig(N, r, cap))
+    assert _fails(tf.test_round_trip_at_the_segment_limit, 256)

@@ -25,6 +25,12 @@ through the library, for the scalar Lloyd-Max codec (k = 1) and FibQuant at k = 
 `--lloyd` times the workload's codebook construction: host numpy Lloyd against GPU Lloyd (the
 library's encoder assigns, `fq_centroid_sums` forms the centroids).
 
+`--archive [--archive-workload document|kv-streams]` times the iterated-map archive of symbol
+streams (the storage layer of "Fractal KV-Cache Archives"): one step encodes every symbol of the
+streams into anchors, decodes them all back and reads a batch of random positions. The metric is
+symbols per second through encode and decode; the line also carries each kernel's rate and the
+latency of one random access and of one appended symbol, each a single launch.
+
 `--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
 sample of the same workload instead.
 
@@ -51,6 +57,13 @@ import synth  # noqa: E402
 
 METRIC = "KV vectors/s encoded and decoded (fp16 GB/s) per bitrate; % of HBM/TC roofline"
 ATTEND_METRIC = "cached KV vectors/s attended (fused decode-into-attention)"
+ARCHIVE_METRIC = "archive symbols/s (encode + decode round trip, with a batch of random accesses)"
+# fp64 arithmetic instructions the archive kernels issue: a forward step is a subtract, a multiply
+# and an add per coordinate; a backward step a subtract and a fused multiply-add per coordinate.
+FA_FWD_FP64, FA_BWD_FP64 = 6, 4
+# fp64 instructions per SM per clock: the nominal 1.25 TFLOP/s of GB300 over 2 flops per fused
+# multiply-add, 152 SMs and the 2070 MHz maximum clock.
+FA_FP64_PER_SM_CLK = 2.0
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -261,23 +274,58 @@ def time_oracle_attend(cfg: int, steps: int) -> dict:
                       f"attended by one query each), {steps} steps, numpy fp64"}
 
 
+def archive_params(N: int) -> tuple[float, int]:
+    """(r, L) of the archive benchmark: r = 3/4 of the disjointness limit sin(pi/N) / (1 + sin(pi/N)),
+    L the longest segment the fp64 error bound allows (the library's own bound)."""
+    import random_access_kv_gb300 as fq
+    r = 0.75 * fq.fa_ratio_limit(N)
+    return r, fq.fa_max_segment(N, r)
+
+
+def time_oracle_archive(name: str, steps: int) -> dict:
+    """The oracle's encode, backward-search decode and random access on a bounded sample: the
+    first segments of the first stream (about 60,000 symbols per step)."""
+    from oracle import fractal as ofa
+    w = synth.ARCHIVE_WORKLOADS[name]
+    r = 0.75 * ofa.ratio_limit(w.N)
+    L = ofa.max_segment(w.N, r)
+    T = min(w.T, 60000)
+    sym = synth.symbol_streams(w.n_streams, w.T, w.N, w.law)[:1, :T]
+    pos = synth.stream_positions(1, T, T, T // 16)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        A = ofa.encode(sym, w.N, r, L)
+        ofa.decode(A, T, w.N, r, L)
+        for p in pos:
+            ofa.access(A, T, w.N, r, L, 0, int(p))
+    dt = time.perf_counter() - t0
+    return {"value": steps * T / dt, "seconds": dt, "symbols": steps * T,
+            "sample": f"the first {T} symbols of workload '{name}' (encoded, decoded, and {T // 16} random "
+                      f"positions read back), {steps} steps, Python fp64"}
+
+
 def run_reference(args) -> None:
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = synth.WORKLOADS[args.workload]
-    timer = time_oracle_attend if args.attend else time_oracle
+    if args.archive:
+        def timer(_, n):
+            return time_oracle_archive(args.archive_workload, n)
+        name, metric, unit = synth.ARCHIVE_WORKLOADS[args.archive_workload].name, ARCHIVE_METRIC, "symbols/s"
+    else:
+        timer = time_oracle_attend if args.attend else time_oracle
+        name, metric, unit = synth.WORKLOADS[args.workload].name, ATTEND_METRIC if args.attend else METRIC, "vectors/s"
     timer(args.workload, max(1, args.warmup))
     r = timer(args.workload, args.steps)
-    cores = host_cores()
+    cores = 1 if args.archive else host_cores()        # the archive oracle is plain Python
     line = {
-        "impl": "reference", "metric": ATTEND_METRIC if args.attend else METRIC, "value": r["value"], "unit": "vectors/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": r["value"], "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * r["seconds"] / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample": r["sample"]},
-        "cpu_baseline": {"value": r["value"], "unit": "vectors/s", "cores": cores, "kind": "oracle",
+        "config": {"workload": name, "sample": r["sample"]},
+        "cpu_baseline": {"value": r["value"], "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": r["sample"]},
-        "e2e": {"value": r["value"], "unit": "vectors/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": r["value"], "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -773,6 +821,203 @@ def run_attend(args) -> None:
         torch.distributed.destroy_process_group()
 
 
+def run_archive(args) -> None:
+    import torch
+    import random_access_kv_gb300 as fq
+    from random_access_kv_gb300 import build as fbuild
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        fbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+
+    w = synth.ARCHIVE_WORKLOADS[args.archive_workload]
+    r, L = archive_params(w.N)
+    ctx = fq.fa_create(w.N, r, L, local)
+    nS, T = w.n_streams, w.T
+    S = fq.fa_segments(ctx, T)
+    sym_np = synth.symbol_streams(nS, T, w.N, w.law)
+    pos_np = synth.stream_positions(nS, T, T, w.lookups)
+    sym_host = torch.from_numpy(sym_np.view(np.int16)).pin_memory()
+    pos_host = torch.from_numpy(pos_np).pin_memory()
+    sym = sym_host.to(dev)
+    pos = pos_host.to(dev)
+    A = fq.alloc_archive(ctx, nS, T, dev)
+    dec = torch.empty((nS, T), dtype=torch.int16, device=dev)
+    acc = torch.empty(w.lookups, dtype=torch.int16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def enc():
+        fq.fa_encode(ctx, sym, nS, T, T, 0, A, sp)
+
+    def dcd():
+        fq.fa_decode(ctx, A, nS, T, T, dec, sp)
+
+    def rnd():
+        fq.fa_access(ctx, A, nS, T, T, pos, w.lookups, acc, sp)
+
+    def step():
+        enc()
+        dcd()
+        rnd()
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if fq.fa_status(ctx, sp) != 0:
+        raise SystemExit("device flags set during warm-up")
+    if not (torch.equal(dec.cpu(), sym_host) and np.array_equal(acc.cpu().numpy(), sym_np[pos_np // T, pos_np % T].view(np.int16))):
+        raise SystemExit("the archive did not return the symbols it stored")
+
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
+    value = job_value(nS * T, args.steps, world, total_ms)
+
+    def timed_alone(fn, reps):
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.mean(ms)
+
+    reps = max(5, args.steps)
+    enc_ms, dec_ms, acc_ms = timed_alone(enc, reps), timed_alone(dcd, reps), timed_alone(rnd, reps)
+
+    # Single-launch latencies, the GPU counterpart of a per-character or per-lookup time: one random
+    # access of one position, and one append of one symbol to each stream (an archive with room).
+    one = pos[:1].clone()
+    lat_acc = timed_alone(lambda: fq.fa_access(ctx, A, nS, T, T, one, 1, acc, sp), 50)
+    extra = 40 + 10 * w.append
+    cap = T + extra
+    A2 = fq.alloc_archive(ctx, nS, cap, dev)
+    fq.fa_encode(ctx, sym, nS, T, cap, 0, A2, sp)
+    tail = torch.from_numpy(synth.symbol_streams(nS, extra, w.N, w.law, sub=1).view(np.int16)).to(dev)
+    cols = [tail[:, i:i + 1].contiguous() for i in range(40)]
+    toks = [tail[:, 40 + i * w.append:40 + (i + 1) * w.append].contiguous() for i in range(10)]
+    done = [T]
+
+    def append(chunk, n):
+        fq.fa_encode(ctx, chunk, nS, n, cap, done[0], A2, sp)
+        done[0] += n
+
+    lat_app = timed_alone(lambda: append(cols[done[0] - T], 1), 40)
+    lat_tok = timed_alone(lambda: append(toks[(done[0] - T - 40) // w.append], w.append), 10)
+    torch.cuda.synchronize(dev)
+    full = torch.cat([sym, tail], dim=1).contiguous()
+    A3 = fq.alloc_archive(ctx, nS, cap, dev)
+    fq.fa_encode(ctx, full, nS, cap, cap, 0, A3, sp)
+    if not torch.equal(A2, A3):
+        raise SystemExit("appended anchors differ from a one-call encode")
+
+    # End to end: the streams come from pinned host memory, the anchors, the decoded streams and the
+    # random-access results go back.
+    a_host = torch.empty_like(A, device="cpu").pin_memory()
+    d_host = torch.empty_like(dec, device="cpu").pin_memory()
+    r_host = torch.empty_like(acc, device="cpu").pin_memory()
+    e2e_ms = []
+    for i in range(args.steps + 3):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sym.copy_(sym_host, non_blocking=True)
+        pos.copy_(pos_host, non_blocking=True)
+        step()
+        a_host.copy_(A, non_blocking=True)
+        d_host.copy_(dec, non_blocking=True)
+        r_host.copy_(acc, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = max_over_ranks(sum(e2e_ms), world, dev)
+    e2e_value = job_value(nS * T, args.steps, world, e2e_total)
+    flags = fq.fa_status(ctx, sp)
+
+    # Roofline: the kernels are chains of dependent fp64 steps, bound by the fp64 pipe.
+    seg_len = np.minimum(L, T - np.arange(S) * L)
+    t_in = pos_np % T
+    acc_steps = int(np.sum(np.minimum(L, T - (t_in // L) * L) - 1 - t_in % L))
+    fp64 = {"encode": FA_FWD_FP64 * nS * T, "decode": FA_BWD_FP64 * nS * int(np.sum(seg_len - 1)),
+            "access": FA_BWD_FP64 * acc_steps}
+    times = {"encode": enc_ms, "decode": dec_ms, "access": acc_ms}
+    dom = max(times, key=times.get)
+    sm_mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    peaks = measured_peaks()
+    peak = peaks["sms"] * FA_FP64_PER_SM_CLK * sm_mhz * 1e6 / 1e12     # T fp64 instructions / s
+    ach = {k: fp64[k] / (times[k] / 1e3) / 1e12 for k in times}
+    roofline = {"kernel": dom, "cuda_kernel": "archive_" + dom, "traffic": None, "bound": "alu",
+                "achieved": round(ach[dom], 4), "peak": round(peak, 4), "unit": "T fp64 instr/s",
+                "frac": round(ach[dom] / peak, 4), "peak_source": "nominal fp64 rate (2 per SM per clock) at the "
+                "sampled SM clock", "fp64_instr_per_launch": fp64[dom], "launch_ms": round(times[dom], 5),
+                "per_kernel": {k: {"ms": round(times[k], 5), "fp64_instr": fp64[k], "frac": round(ach[k] / peak, 4)}
+                               for k in times}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c = time_oracle_archive(args.archive_workload, args.cpu_steps)
+        cpu = {"value": c["value"], "unit": "symbols/s", "cores": 1, "kind": "oracle", "sample": c["sample"],
+               "seconds": round(c["seconds"], 2)}
+    if rank == 0:
+        line = {
+            "metric": ARCHIVE_METRIC, "value": value, "unit": "symbols/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "n_streams": nS, "T": T, "N": w.N, "r": r, "L": L,
+                       "lookups_per_step": w.lookups, "anchor_bits_per_symbol": round(128 / L, 3),
+                       "raw_bits_per_symbol": float(np.log2(w.N)),
+                       "l2": "flushed before every timed step (256 MB write, outside the step events)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "rates": {"encode_symbols_per_s": nS * T / (enc_ms / 1e3), "decode_symbols_per_s": nS * T / (dec_ms / 1e3),
+                      "access_lookups_per_s": w.lookups / (acc_ms / 1e3),
+                      "encode_ns_per_symbol": 1e6 * enc_ms / (nS * T),
+                      "access_us_single_lookup": 1e3 * lat_acc,
+                      "append_us_one_symbol_per_stream": 1e3 * lat_app,
+                      "append_us_one_token": 1e3 * lat_tok, "token_symbols_per_stream": w.append},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "symbols/s",
+                    "h2d_bytes_per_step": int(sym_host.numel() * 2 + pos_host.numel() * 8),
+                    "d2h_bytes_per_step": int(a_host.numel() * 8 + d_host.numel() * 2 + r_host.numel() * 2)},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+            "device_flags": flags,
+        }
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # Rate sweep: (codec, k, N) points at d = 64; b = log2(N) / k bits per coordinate.
 SWEEP_POINTS = ([("scalar", 1, n) for n in (2, 4, 8, 16)]
                 + [("fibquant", 2, n) for n in (4, 8, 16, 32, 64, 128, 256)]
@@ -930,10 +1175,13 @@ def main():
                     help="with --attend: queries per cached (layer, head) group (grouped-query attention)")
     ap.add_argument("--groups", type=int, default=0,
                     help="with --attend: the first G (layer, head) groups only (a small case for profiling)")
+    ap.add_argument("--archive", action="store_true",
+                    help="time the iterated-map archive of symbol streams (encode, decode, random access)")
+    ap.add_argument("--archive-workload", choices=sorted(synth.ARCHIVE_WORKLOADS), default="document")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0,
                     help="rows per tensor (a prefix of the workload; a small case for profiling). "
-                         "Not for the streaming workload.")
+                         "A multiple of the sequence length for the streaming workload.")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
@@ -943,6 +1191,8 @@ def main():
         run_rate_sweep(args)
     elif args.lloyd:
         run_lloyd(args)
+    elif args.archive:
+        run_archive(args)
     elif args.attend:
         run_attend(args)
     else:

@@ -1,4 +1,4 @@
-"""ctypes binding of libfq.so: the C ABI of include/fq.h under the same names.
+"""ctypes binding of libfq.so: the C ABI of include/fq.h and include/fractal.h under the same names.
 
 Argument marshalling only: every function takes device buffers as torch CUDA tensors (or raw
 integer addresses), passes their addresses and sizes to the C entry point of the same name and
@@ -15,10 +15,11 @@ import re
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfq.so")
-HEADER = os.path.join(os.path.dirname(PKG), "include", "fq.h")
+HEADERS = [os.path.join(os.path.dirname(PKG), "include", h) for h in ("fq.h", "fractal.h")]
 
 FQ_OK, FQ_EINVAL, FQ_ENOMEM, FQ_ECUDA, FQ_EALIGN, FQ_ENODEV = range(6)
 FQ_FLAG_RANGE, FQ_FLAG_NONFINITE, FQ_FLAG_TIMEOUT = 1, 2, 4
+FA_FLAG_SYMBOL, FA_FLAG_RANGE, FA_FLAG_CORRUPT = 1, 2, 4
 
 
 class FQLibraryMissing(ImportError):
@@ -50,17 +51,30 @@ _SIGNATURES = {
     "fq_status": (_int, [_c_void_p, _c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "fq_destroy": (None, [_c_void_p]),
     "fq_strerror": (ctypes.c_char_p, [_int]),
+    "fa_ratio_limit": (ctypes.c_double, [_int]),
+    "fa_max_segment": (_int, [_int, ctypes.c_double]),
+    "fa_create": (_int, [ctypes.POINTER(_c_void_p), _int, ctypes.c_double, _int, _int]),
+    "fa_params": (_int, [_c_void_p, ctypes.POINTER(_int), ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_int)]),
+    "fa_vertex_table": (_int, [_c_void_p, _c_void_p]),
+    "fa_segments": (_i64, [_c_void_p, _i64]),
+    "fa_encode": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _i64, _c_void_p, _c_void_p]),
+    "fa_decode": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p]),
+    "fa_access": (_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _i64, _c_void_p, _c_void_p]),
+    "fa_status": (_int, [_c_void_p, _c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "fa_destroy": (None, [_c_void_p]),
 }
 
 _lib = None
 
 
 def header_symbols() -> list[str]:
-    """Names of the functions declared in include/fq.h."""
-    with open(HEADER) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(fq_[a-z0-9_]+)\s*\(", text)))
+    """Names of the functions declared in include/fq.h and include/fractal.h."""
+    names = set()
+    for h in HEADERS:
+        with open(h) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        names.update(re.findall(r"\b((?:fq|fa)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def lib() -> ctypes.CDLL:
@@ -111,6 +125,8 @@ def _check(fn: str, rc: int) -> None:
 class Context:
     """Owns an ``fq_ctx*``; frees it with ``fq_destroy`` on ``close()`` or garbage collection."""
 
+    _destroy = "fq_destroy"
+
     def __init__(self, handle: int):
         self.handle = handle
 
@@ -120,7 +136,7 @@ class Context:
 
     def close(self) -> None:
         if self.handle:
-            lib().fq_destroy(ctypes.c_void_p(self.handle))
+            getattr(lib(), self._destroy)(ctypes.c_void_p(self.handle))
             self.handle = 0
 
     def __del__(self):
@@ -215,3 +231,74 @@ def fq_destroy(ctx: Context) -> None:
 
 def fq_strerror(code: int) -> str:
     return strerror(code)
+
+
+# Iterated-map archive of symbol streams (include/fractal.h).
+
+class ArchiveContext(Context):
+    """Owns an ``fa_ctx*``; frees it with ``fa_destroy``."""
+
+    _destroy = "fa_destroy"
+
+
+def fa_ratio_limit(N: int) -> float:
+    return float(lib().fa_ratio_limit(int(N)))
+
+
+def fa_max_segment(N: int, r: float) -> int:
+    return int(lib().fa_max_segment(int(N), float(r)))
+
+
+def fa_create(N: int, r: float, L: int, device: int = 0) -> ArchiveContext:
+    h = _c_void_p()
+    _check("fa_create", lib().fa_create(ctypes.byref(h), int(N), float(r), int(L), int(device)))
+    return ArchiveContext(h.value)
+
+
+def fa_params(ctx: ArchiveContext) -> tuple[int, float, int]:
+    N, r, L = _int(), ctypes.c_double(), _int()
+    _check("fa_params", lib().fa_params(ctx, ctypes.byref(N), ctypes.byref(r), ctypes.byref(L)))
+    return N.value, r.value, L.value
+
+
+def fa_vertex_table(ctx: ArchiveContext):
+    """The context's vertex table as a float64 numpy array [N, 2]."""
+    import numpy as np
+    N, _, _ = fa_params(ctx)
+    V = np.zeros((N, 2), dtype=np.float64)
+    _check("fa_vertex_table", lib().fa_vertex_table(ctx, V.ctypes.data))
+    return V
+
+
+def fa_segments(ctx: ArchiveContext, T_cap: int) -> int:
+    s = lib().fa_segments(ctx, int(T_cap))
+    if s < 0:
+        raise FQError("fa_segments", FQ_EINVAL)
+    return int(s)
+
+
+def fa_encode(ctx: ArchiveContext, sym, n_streams: int, n_new: int, T_cap: int, T_old: int, anchors,
+              stream=None) -> None:
+    _check("fa_encode", lib().fa_encode(ctx, _ptr(sym), int(n_streams), int(n_new), int(T_cap), int(T_old),
+                                        _ptr(anchors), _stream(stream)))
+
+
+def fa_decode(ctx: ArchiveContext, anchors, n_streams: int, T_cap: int, T: int, out, stream=None) -> None:
+    _check("fa_decode", lib().fa_decode(ctx, _ptr(anchors), int(n_streams), int(T_cap), int(T), _ptr(out),
+                                        _stream(stream)))
+
+
+def fa_access(ctx: ArchiveContext, anchors, n_streams: int, T_cap: int, T: int, pos, n: int, out,
+              stream=None) -> None:
+    _check("fa_access", lib().fa_access(ctx, _ptr(anchors), int(n_streams), int(T_cap), int(T), _ptr(pos), int(n),
+                                        _ptr(out), _stream(stream)))
+
+
+def fa_status(ctx: ArchiveContext, stream=None) -> int:
+    f = ctypes.c_uint32()
+    _check("fa_status", lib().fa_status(ctx, _stream(stream), ctypes.byref(f)))
+    return int(f.value)
+
+
+def fa_destroy(ctx: ArchiveContext) -> None:
+    ctx.close()

@@ -1,0 +1,371 @@
+// Iterated-map archive of symbol streams ("Fractal KV-Cache Archives", Method 1): encode / append,
+// full decode and random access, with the C ABI of include/fractal.h.
+//
+// Each segment of L symbols is independent (it starts at the origin), so one device thread owns one
+// segment (encode, decode) or one lookup (random access). The work is a chain of dependent fp64
+// steps per thread: GB300 runs fp64 at a small fraction of its fp32 rate, so these kernels are
+// bound by the fp64 pipe, not by memory (2 bytes per symbol in, 16 bytes per segment out).
+//   * forward step, per coordinate: t = p - V, t = r t, p = V + t, each operation rounded (no
+//     contraction into a fused multiply-add), which makes anchors identical whatever the split of a
+//     stream into append calls;
+//   * backward step: the cell is found in fp32 (the angle of the point rounded to the nearest
+//     vertex; the cells are disjoint with a margin the context guarantees to be at least 2e-5, far
+//     above fp32 error), the point is checked to lie within r + 3/4 of the margin of that cell's
+//     centre, then the map is inverted in fp64 as p = V + (p - V) / r with the quotient taken as a
+//     fused multiply by 1/r.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <vector>
+
+#include "fractal.h"
+
+struct fa_ctx {
+    int device = 0;
+    int N = 0;
+    int L = 0;
+    double r = 0.0;
+    double rinv = 0.0;
+    float scaleN = 0.f;     // N / (2 pi): angle to vertex index
+    float lim2 = 0.f;       // (r + 3/4 margin)^2: largest squared distance to a cell centre
+    double2 *V = nullptr;   // [N] vertices
+    float2 *Cf = nullptr;   // [N] cell centres (1 - r) V(c), fp32
+    uint32_t *flags = nullptr;
+};
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr uint16_t kBad = 0xFFFFu;
+constexpr int kMaxN = 4096;
+constexpr int kMaxSegment = 64;
+constexpr double kMinMargin = 2e-5;
+
+struct Tables {
+    const double2 *V;
+    const float2 *Cf;
+    int N;
+    int L;
+    double r;
+    double rinv;
+    float scaleN;
+    float lim2;
+    uint32_t *flags;
+};
+
+Tables tables_of(const fa_ctx *c) {
+    return Tables{c->V, c->Cf, c->N, c->L, c->r, c->rinv, c->scaleN, c->lim2, c->flags};
+}
+
+__device__ __forceinline__ void forward_step(double &x, double &y, double2 v, double r) {
+    x = __dadd_rn(v.x, __dmul_rn(r, __dsub_rn(x, v.x)));
+    y = __dadd_rn(v.y, __dmul_rn(r, __dsub_rn(y, v.y)));
+}
+
+__device__ __forceinline__ void backward_step(double &x, double &y, double2 v, double rinv) {
+    x = __fma_rn(__dsub_rn(x, v.x), rinv, v.x);
+    y = __fma_rn(__dsub_rn(y, v.y), rinv, v.y);
+}
+
+// The symbol whose cell holds (x, y); sets `bad` when the point is not within reach of that cell
+// (NaN included). Returns the vertex in v.
+__device__ __forceinline__ int find_cell(double x, double y, const Tables &t, double2 &v, bool &bad) {
+    const float fx = __double2float_rn(x), fy = __double2float_rn(y);
+    int c = __float2int_rn(atan2f(fy, fx) * t.scaleN);
+    if (c < 0) c += t.N;
+    c = min(max(c, 0), t.N - 1);
+    const float2 ctr = __ldg(t.Cf + c);
+    const float dx = fx - ctr.x, dy = fy - ctr.y;
+    if (!(fmaf(dx, dx, dy * dy) <= t.lim2)) bad = true;
+    v = __ldg(t.V + c);
+    return c;
+}
+
+// One thread per touched segment (stream q, segment s0 + j): continue or start the segment with the
+// appended symbols at positions [max(s L, T_old), min(s L + L, T_old + n_new)).
+__global__ void __launch_bounds__(kThreads)
+archive_encode(Tables t, const uint16_t *__restrict__ sym, int64_t n_streams, int64_t n_new, int64_t S_cap,
+               int64_t T_old, int64_t s0, int64_t n_seg, double2 *__restrict__ anchors) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_streams * n_seg) return;
+    const int64_t q = i / n_seg, s = s0 + (i - q * n_seg);
+    int64_t lo = s * t.L;
+    int64_t hi = lo + t.L;
+    if (hi > T_old + n_new) hi = T_old + n_new;
+    double2 *a = anchors + q * S_cap + s;
+    double x = 0.0, y = 0.0;
+    if (lo < T_old) {               // the partial last segment continues from its stored point
+        const double2 p = *a;
+        x = p.x;
+        y = p.y;
+        lo = T_old;
+    }
+    const uint16_t *src = sym + q * n_new;
+    bool bad = false;
+    for (int64_t pos = lo; pos < hi; ++pos) {
+        uint32_t c = src[pos - T_old];
+        if (c >= (uint32_t)t.N) {
+            bad = true;
+            c = 0;
+        }
+        forward_step(x, y, __ldg(t.V + c), t.r);
+    }
+    if (bad) {
+        x = y = __longlong_as_double(0x7ff8000000000000LL);
+        atomicOr(t.flags, (uint32_t)FA_FLAG_SYMBOL);
+    }
+    *a = make_double2(x, y);
+}
+
+// One thread per segment: every symbol, from the last position back to the first.
+__global__ void __launch_bounds__(kThreads)
+archive_decode(Tables t, const double2 *__restrict__ anchors, int64_t n_streams, int64_t S_cap, int64_t T,
+               int64_t S, uint16_t *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n_streams * S) return;
+    const int64_t q = i / S, s = i - q * S;
+    const int len = (int)min((int64_t)t.L, T - s * t.L);
+    const double2 p = anchors[q * S_cap + s];
+    double x = p.x, y = p.y;
+    uint16_t *o = out + q * T + s * t.L;
+    bool bad = false;
+    for (int k = len - 1; k >= 0; --k) {
+        double2 v;
+        const int c = find_cell(x, y, t, v, bad);
+        o[k] = bad ? kBad : (uint16_t)c;
+        if (k) backward_step(x, y, v, t.rinv);
+    }
+    if (bad) atomicOr(t.flags, (uint32_t)FA_FLAG_CORRUPT);
+}
+
+// One thread per lookup: backward from the segment's anchor down to the wanted position only.
+__global__ void __launch_bounds__(kThreads)
+archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams, int64_t T_cap, int64_t S_cap,
+               int64_t T, const int64_t *__restrict__ pos, int64_t n, uint16_t *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int64_t g = pos[i];
+    const int64_t q = g >= 0 ? g / T_cap : -1;
+    const int64_t tt = g - q * T_cap;
+    if (g < 0 || q >= n_streams || tt >= T) {
+        out[i] = kBad;
+        atomicOr(t.flags, (uint32_t)FA_FLAG_RANGE);
+        return;
+    }
+    const int64_t s = tt / t.L;
+    const int off = (int)(tt - s * t.L);
+    const int len = (int)min((int64_t)t.L, T - s * t.L);
+    const double2 p = anchors[q * S_cap + s];
+    double x = p.x, y = p.y;
+    bool bad = false;
+    int c = 0;
+    for (int k = len - 1;; --k) {
+        double2 v;
+        c = find_cell(x, y, t, v, bad);
+        if (k <= off) break;
+        backward_step(x, y, v, t.rinv);
+    }
+    out[i] = bad ? kBad : (uint16_t)c;
+    if (bad) atomicOr(t.flags, (uint32_t)FA_FLAG_CORRUPT);
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    cudaError_t err = cudaSuccess;
+    explicit DeviceGuard(int dev) {
+        err = cudaGetDevice(&prev);
+        if (err == cudaSuccess && prev != dev) {
+            err = cudaSetDevice(dev);
+            changed = err == cudaSuccess;
+        }
+    }
+    ~DeviceGuard() {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+double cell_margin(int N, double r) { return (1.0 - r) * sin(M_PI / N) - r; }
+
+void free_ctx(fa_ctx *c) {
+    if (!c) return;
+    cudaFree(c->V);
+    cudaFree(c->Cf);
+    cudaFree(c->flags);
+    delete c;
+}
+
+unsigned blocks_for(int64_t threads) { return (unsigned)((threads + kThreads - 1) / kThreads); }
+
+}  // namespace
+
+extern "C" {
+
+double fa_ratio_limit(int N) {
+    if (N < 2) return 0.0;
+    const double s = sin(M_PI / N);
+    return s / (1.0 + s);
+}
+
+int fa_max_segment(int N, double r) {
+    if (N < 2 || !(r > 0.0) || !(r < fa_ratio_limit(N))) return 0;
+    const double u = ldexp(1.0, -53);
+    const double half_margin = 0.5 * cell_margin(N, r);
+    const double delta = 1.01 * u * (1.0 + 4.0 * r);     // forward step, per coordinate
+    const double eta = 8.0 * u;                           // backward step, per coordinate
+    // error bound of the rebuilt point after j backward steps: sqrt(2) (delta + r eta) r^-j / (1 - r)
+    double err = sqrt(2.0) * (delta + r * eta) / (1.0 - r);
+    if (!(err <= half_margin)) return 0;
+    int L = 1;                                            // decisions j = 0 .. L-1 all fit
+    while (L < kMaxSegment && err / r <= half_margin) {
+        err /= r;
+        ++L;
+    }
+    return L;
+}
+
+int fa_create(fa_ctx **out, int N, double r, int L, int device) {
+    if (!out) return FQ_EINVAL;
+    *out = nullptr;
+    if (N < 2 || N > kMaxN || !isfinite(r) || !(r > 0.0) || !(r < fa_ratio_limit(N))) return FQ_EINVAL;
+    if (cell_margin(N, r) < kMinMargin || L < 1 || L > fa_max_segment(N, r)) return FQ_EINVAL;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return FQ_ENODEV;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return FQ_ENODEV;
+    if (prop.major != 10 || prop.minor != 3) return FQ_ENODEV;
+    DeviceGuard g(device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+
+    fa_ctx *c = new fa_ctx();
+    c->device = device;
+    c->N = N;
+    c->L = L;
+    c->r = r;
+    c->rinv = 1.0 / r;
+    c->scaleN = (float)(N / (2.0 * M_PI));
+    const double lim = r + 0.75 * cell_margin(N, r);
+    c->lim2 = (float)(lim * lim);
+    std::vector<double2> V(N);
+    std::vector<float2> Cf(N);
+    for (int k = 0; k < N; ++k) {
+        const double a = 2.0 * M_PI * k / N;
+        V[k] = make_double2(cos(a), sin(a));
+        Cf[k] = make_float2((float)((1.0 - r) * V[k].x), (float)((1.0 - r) * V[k].y));
+    }
+    cudaError_t e = cudaMalloc((void **)&c->V, sizeof(double2) * N);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&c->Cf, sizeof(float2) * N);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        free_ctx(c);
+        return e == cudaErrorMemoryAllocation ? FQ_ENOMEM : FQ_ECUDA;
+    }
+    e = cudaMemcpy(c->V, V.data(), sizeof(double2) * N, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(c->Cf, Cf.data(), sizeof(float2) * N, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) {
+        free_ctx(c);
+        return FQ_ECUDA;
+    }
+    *out = c;
+    return FQ_OK;
+}
+
+int fa_params(const fa_ctx *ctx, int *N, double *r, int *L) {
+    if (!ctx) return FQ_EINVAL;
+    if (N) *N = ctx->N;
+    if (r) *r = ctx->r;
+    if (L) *L = ctx->L;
+    return FQ_OK;
+}
+
+int fa_vertex_table(const fa_ctx *ctx, double *V_host) {
+    if (!ctx || !V_host) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    return cudaMemcpy(V_host, ctx->V, sizeof(double2) * ctx->N, cudaMemcpyDeviceToHost) == cudaSuccess ? FQ_OK
+                                                                                                         : FQ_ECUDA;
+}
+
+int64_t fa_segments(const fa_ctx *ctx, int64_t T_cap) {
+    if (!ctx || T_cap < 1) return -1;
+    return (T_cap + ctx->L - 1) / ctx->L;
+}
+
+int fa_encode(fa_ctx *ctx, const uint16_t *sym, int64_t n_streams, int64_t n_new, int64_t T_cap, int64_t T_old,
+              double *anchors, void *stream) {
+    if (!ctx || n_streams < 0 || n_new < 0 || T_cap < 1 || T_old < 0 || T_old > T_cap - n_new) return FQ_EINVAL;
+    if (n_streams == 0 || n_new == 0) return FQ_OK;
+    if (!sym || !anchors) return FQ_EINVAL;
+    if (!aligned(sym, 2) || !aligned(anchors, 16)) return FQ_EALIGN;
+    const int64_t S_cap = fa_segments(ctx, T_cap);
+    const int64_t s0 = T_old / ctx->L, n_seg = (T_old + n_new - 1) / ctx->L - s0 + 1;
+    if (n_streams > INT64_MAX / S_cap || n_streams > INT64_MAX / n_new) return FQ_EINVAL;
+    const int64_t threads = n_streams * n_seg;
+    if ((threads + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    archive_encode<<<blocks_for(threads), kThreads, 0, (cudaStream_t)stream>>>(
+        tables_of(ctx), sym, n_streams, n_new, S_cap, T_old, s0, n_seg, reinterpret_cast<double2 *>(anchors));
+    return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
+int fa_decode(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_cap, int64_t T, uint16_t *out,
+              void *stream) {
+    if (!ctx || n_streams < 0 || T_cap < 1 || T < 0 || T > T_cap) return FQ_EINVAL;
+    if (n_streams == 0 || T == 0) return FQ_OK;
+    if (!anchors || !out) return FQ_EINVAL;
+    if (!aligned(anchors, 16) || !aligned(out, 2)) return FQ_EALIGN;
+    const int64_t S_cap = fa_segments(ctx, T_cap), S = (T + ctx->L - 1) / ctx->L;
+    if (n_streams > INT64_MAX / S_cap || n_streams > INT64_MAX / T) return FQ_EINVAL;
+    const int64_t threads = n_streams * S;
+    if ((threads + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    archive_decode<<<blocks_for(threads), kThreads, 0, (cudaStream_t)stream>>>(
+        tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, S_cap, T, S, out);
+    return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
+int fa_access(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_cap, int64_t T, const int64_t *pos,
+              int64_t n, uint16_t *out, void *stream) {
+    if (!ctx || n_streams < 0 || T_cap < 1 || T < 0 || T > T_cap || n < 0) return FQ_EINVAL;
+    if (n == 0) return FQ_OK;
+    if (!pos || !out || (!anchors && n_streams > 0 && T > 0)) return FQ_EINVAL;
+    if (!aligned(anchors, 16) || !aligned(pos, 8) || !aligned(out, 2)) return FQ_EALIGN;
+    const int64_t S_cap = fa_segments(ctx, T_cap);
+    if (n_streams > INT64_MAX / T_cap || n_streams > INT64_MAX / S_cap) return FQ_EINVAL;
+    if ((n + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    archive_access<<<blocks_for(n), kThreads, 0, (cudaStream_t)stream>>>(
+        tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, T_cap, S_cap, T, pos, n, out);
+    return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
+}
+
+int fa_status(fa_ctx *ctx, void *stream, uint32_t *flags) {
+    if (!ctx || !flags) return FQ_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (g.err != cudaSuccess) return FQ_ECUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, ctx->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flags, 0, sizeof(uint32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return FQ_ECUDA;
+    *flags = h;
+    return FQ_OK;
+}
+
+void fa_destroy(fa_ctx *ctx) {
+    if (!ctx) return;
+    DeviceGuard g(ctx->device);
+    cudaDeviceSynchronize();
+    free_ctx(ctx);
+}
+
+}  // extern "C"

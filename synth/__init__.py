@@ -14,7 +14,11 @@ distributions described per workload below.
 Random streams: ``rng(cfg, stream, *sub)`` is ``numpy.random.default_rng([cfg, stream, *sub])``.
 Stream 0 = K data, 1 = V data, 2 = the Gaussian matrix behind the rotation, 3 = codebook
 building (Lloyd training draws, restart rotations, Kronecker offset), 4 = gather indices,
-5 = attention queries, 6 = random code stores.
+5 = attention queries, 6 = random code stores, 7 = symbol streams for the iterated-map archive.
+
+The archive workloads (``ARCHIVE_WORKLOADS``) stand in for the inputs of the page "Fractal KV-Cache
+Archives" (gist.science summary of arXiv 2607.07144), whose codec timings are quoted on a document
+of a million characters: a byte stream with a text-like skew, and the index streams of a KV cache.
 """
 from __future__ import annotations
 
@@ -24,7 +28,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 STREAM_K, STREAM_V, STREAM_ROT, STREAM_CODEBOOK, STREAM_GATHER = 0, 1, 2, 3, 4
-STREAM_QUERY, STREAM_STORE = 5, 6
+STREAM_QUERY, STREAM_STORE, STREAM_SYMBOLS = 5, 6, 7
 
 
 def rng(cfg: int, stream: int, *sub: int) -> np.random.Generator:
@@ -200,3 +204,43 @@ def random_store(cfg: int, M: int, n_words: int, sub: int = 0) -> tuple[np.ndarr
     nu = np.exp(r.normal(np.log(8.0), 0.5, size=M)).astype(np.float32)
     words = r.integers(0, 1 << 32, size=n_words, dtype=np.uint64).astype(np.uint32)
     return nu, words
+
+
+@dataclass(frozen=True)
+class ArchiveWorkload:
+    """Symbol streams for the iterated-map archive: n_streams streams of T symbols over N."""
+
+    name: str
+    n_streams: int
+    T: int
+    N: int
+    law: str            # "zipf": p(c) proportional to (c + 1)^-1.1; "uniform"
+    append: int         # symbols per stream per append call in the streaming measurement
+    lookups: int        # random-access positions per step
+
+
+ARCHIVE_WORKLOADS = {
+    "document": ArchiveWorkload("document: 1 stream of 2^20 bytes, N=256, Zipf(1.1)", 1, 1 << 20, 256, "zipf",
+                                1, 1 << 20),
+    "kv-streams": ArchiveWorkload("KV index streams: 144 (layer, head) streams x 1024 tokens x 32 indices, N=256",
+                                  144, 32768, 256, "uniform", 32, 1 << 20),
+}
+
+
+def symbol_streams(n_streams: int, T: int, N: int, law: str = "uniform", sub: int = 0) -> np.ndarray:
+    """uint16 [n_streams, T] symbols in [0, N) (stream 7). ``zipf`` draws symbol c with probability
+    proportional to (c + 1)^-1.1, the skew of characters in text; ``uniform`` suits codec indices,
+    which a well-built codebook makes close to equiprobable."""
+    r = rng(N, STREAM_SYMBOLS, n_streams, T, sub)
+    if law == "uniform":
+        return r.integers(0, N, size=(n_streams, T), dtype=np.int64).astype(np.uint16)
+    if law == "zipf":
+        p = 1.0 / np.arange(1, N + 1, dtype=np.float64) ** 1.1
+        return r.choice(N, size=(n_streams, T), p=p / p.sum()).astype(np.uint16)
+    raise ValueError(law)
+
+
+def stream_positions(n_streams: int, T_cap: int, T: int, n: int, sub: int = 0) -> np.ndarray:
+    """n flat positions q T_cap + t (stream q < n_streams, position t < T), uniform (stream 7)."""
+    r = rng(n_streams, STREAM_SYMBOLS, T, n, 1000 + sub)
+    return r.integers(0, n_streams, size=n) * int(T_cap) + r.integers(0, T, size=n)

@@ -70,3 +70,36 @@ def test_codebook_load_without_gpu_reports_no_device(L):
         pytest.skip("a GPU is present")
     rc, h = _load(L, np.zeros((16, 2)), np.eye(64))
     assert rc == fb.FQ_ENODEV and not h
+
+
+def test_archive_null_context_and_host_checks(L):
+    assert L.fa_segments(None, 10) == -1
+    assert L.fa_params(None, None, None, None) == fb.FQ_EINVAL
+    assert L.fa_vertex_table(None, None) == fb.FQ_EINVAL
+    assert L.fa_encode(None, None, 1, 4, 8, 0, None, None) == fb.FQ_EINVAL
+    assert L.fa_decode(None, None, 1, 8, 8, None, None) == fb.FQ_EINVAL
+    assert L.fa_access(None, None, 1, 8, 8, None, 1, None, None) == fb.FQ_EINVAL
+    assert L.fa_status(None, None, None) == fb.FQ_EINVAL
+    L.fa_destroy(None)
+    h = ctypes.c_void_p()
+    # parameter checks answer before any device is touched
+    assert L.fa_create(ctypes.byref(h), 1, 0.1, 4, 0) == fb.FQ_EINVAL and not h.value
+    assert L.fa_create(ctypes.byref(h), 8192, 1e-4, 2, 0) == fb.FQ_EINVAL
+    assert L.fa_create(ctypes.byref(h), 16, 0.2, 4, 0) == fb.FQ_EINVAL        # r above the limit
+    assert L.fa_create(ctypes.byref(h), 16, float("nan"), 4, 0) == fb.FQ_EINVAL
+    r = 0.75 * L.fa_ratio_limit(16)
+    assert L.fa_create(ctypes.byref(h), 16, r, L.fa_max_segment(16, r) + 1, 0) == fb.FQ_EINVAL
+    assert L.fa_create(ctypes.byref(h), 16, r, 0, 0) == fb.FQ_EINVAL
+    assert L.fa_create(None, 16, r, 4, 0) == fb.FQ_EINVAL
+
+
+def test_archive_limits_match_the_oracle(L):
+    # The disjointness limit and the segment-length bound are host arithmetic, stated in the library
+    # and (separately) in the oracle; both must give the same lengths.
+    from oracle import fractal as ofa
+    for N in (2, 3, 4, 5, 16, 64, 100, 256, 1000, 4096):
+        assert L.fa_ratio_limit(N) == pytest.approx(ofa.ratio_limit(N), rel=1e-15)
+        for rho in (0.1, 0.25, 0.5, 0.6, 0.75, 0.9, 0.99, 1.0, 1.2):
+            r = rho * ofa.ratio_limit(N)
+            assert L.fa_max_segment(N, r) == ofa.max_segment(N, r), (N, rho)
+    assert L.fa_ratio_limit(1) == 0.0 and L.fa_max_segment(1, 0.1) == 0 and L.fa_max_segment(8, -0.1) == 0

@@ -12,7 +12,9 @@
 //     vertex; the cells are disjoint with a margin the context guarantees to be at least 2e-5, far
 //     above fp32 error), the point is checked to lie within r + 3/4 of the margin of that cell's
 //     centre, then the map is inverted in fp64 as p = V + (p - V) / r with the quotient taken as a
-//     fused multiply by 1/r.
+//     fused multiply by 1/r. The fp32 copy of the point is cut from the fp64 bits with integer
+//     instructions: a hardware fp64-to-fp32 conversion would take fp64 pipe cycles, which are
+//     the scarce resource here.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -30,6 +32,7 @@ struct fa_ctx {
     double rinv = 0.0;
     float scaleN = 0.f;     // N / (2 pi): angle to vertex index
     float lim2 = 0.f;       // (r + 3/4 margin)^2: largest squared distance to a cell centre
+    int num_sms = 0;
     double2 *V = nullptr;   // [N] vertices
     float2 *Cf = nullptr;   // [N] cell centres (1 - r) V(c), fp32
     uint32_t *flags = nullptr;
@@ -69,10 +72,24 @@ __device__ __forceinline__ void backward_step(double &x, double &y, double2 v, d
     y = __fma_rn(__dsub_rn(y, v.y), rinv, v.y);
 }
 
+// x as an fp32 number with its mantissa truncated to 23 bits (relative error below 2^-23), from
+// the IEEE-754 fields: magnitudes below the fp32 normal range become zero; infinities and NaNs stay
+// infinities and NaNs.
+__device__ __forceinline__ float to_f32_trunc(double x) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+    const uint32_t hi = (uint32_t)(b >> 32);
+    const uint32_t sign = hi & 0x80000000u;
+    const int e = (int)((hi >> 20) & 0x7ffu) - 1023 + 127;
+    const uint32_t m = (uint32_t)(b >> 29) & 0x7fffffu;
+    if (e <= 0) return __uint_as_float(sign);
+    if (e >= 255) return __uint_as_float(sign | 0x7f800000u | (m ? 0x400000u : 0u));
+    return __uint_as_float(sign | ((uint32_t)e << 23) | m);
+}
+
 // The symbol whose cell holds (x, y); sets `bad` when the point is not within reach of that cell
 // (NaN included). Returns the vertex in v.
 __device__ __forceinline__ int find_cell(double x, double y, const Tables &t, double2 &v, bool &bad) {
-    const float fx = __double2float_rn(x), fy = __double2float_rn(y);
+    const float fx = to_f32_trunc(x), fy = to_f32_trunc(y);
     int c = __float2int_rn(atan2f(fy, fx) * t.scaleN);
     if (c < 0) c += t.N;
     c = min(max(c, 0), t.N - 1);
@@ -102,15 +119,27 @@ archive_encode(Tables t, const uint16_t *__restrict__ sym, int64_t n_streams, in
         y = p.y;
         lo = T_old;
     }
-    const uint16_t *src = sym + q * n_new;
+    const uint16_t *row = sym + q * n_new;
+    auto src = [&](int64_t p) -> uint32_t { return row[p - T_old]; };   // the symbol at position p
     bool bad = false;
-    for (int64_t pos = lo; pos < hi; ++pos) {
-        uint32_t c = src[pos - T_old];
+    // The loads of a step do not depend on the point, so they run ahead of the fp64 chain: the
+    // symbol two steps ahead and the vertex one step ahead.
+    auto vertex = [&](uint32_t c) {
         if (c >= (uint32_t)t.N) {
             bad = true;
             c = 0;
         }
-        forward_step(x, y, __ldg(t.V + c), t.r);
+        return __ldg(t.V + c);
+    };
+    uint32_t c_next = lo + 1 < hi ? src(lo + 1) : 0u;
+    double2 v = lo < hi ? vertex(src(lo)) : make_double2(0.0, 0.0);
+    for (int64_t pos = lo; pos < hi; ++pos) {
+        const double2 vc = v;
+        if (pos + 1 < hi) {
+            v = vertex(c_next);
+            if (pos + 2 < hi) c_next = src(pos + 2);
+        }
+        forward_step(x, y, vc, t.r);
     }
     if (bad) {
         x = y = __longlong_as_double(0x7ff8000000000000LL);
@@ -140,35 +169,132 @@ archive_decode(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
     if (bad) atomicOr(t.flags, (uint32_t)FA_FLAG_CORRUPT);
 }
 
-// One thread per lookup: backward from the segment's anchor down to the wanted position only.
+// Random access: backward from each lookup's segment anchor down to the wanted position only.
+//
+// A lookup needs between 0 and L - 1 backward steps, so one lookup per thread would leave most lanes
+// of a warp idle while the longest walk finishes, and every fp64 instruction costs the pipe the same
+// whatever its active lanes. Instead each warp owns a run of `per_warp` lookups as a queue: a lane
+// that answers its lookup takes the next one (its first decision in the same round), so the fp64
+// backward step of every round is shared by most lanes (about 3/4 of them with 8 lookups per lane,
+// 4/5 with 16, for walks of 0 .. 6 steps). Each lane keeps two lookups in flight behind the current
+// one: slot A with its anchor load issued, slot B with its position loaded; the queue hands out B
+// slots once per round through a warp ballot.
+constexpr int kAccessMinPerLane = 4;
+constexpr int kAccessMaxPerLane = 16;
+constexpr int kAccessWarpsPerSm = 24;
+
 __global__ void __launch_bounds__(kThreads)
 archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams, int64_t T_cap, int64_t S_cap,
-               int64_t T, const int64_t *__restrict__ pos, int64_t n, uint16_t *__restrict__ out) {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const int64_t g = pos[i];
-    const int64_t q = g >= 0 ? g / T_cap : -1;
-    const int64_t tt = g - q * T_cap;
-    if (g < 0 || q >= n_streams || tt >= T) {
-        out[i] = kBad;
-        atomicOr(t.flags, (uint32_t)FA_FLAG_RANGE);
-        return;
+               int64_t T, const int64_t *__restrict__ pos, int64_t n, int per_warp, uint16_t *__restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t begin = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * per_warp;
+    if (begin >= n) return;                                      // uniform over the warp
+    const int64_t end = min(n, begin + per_warp);
+    const unsigned below = (1u << lane) - 1u;
+    int64_t head = begin;                                        // next unclaimed lookup (warp-uniform)
+
+    int64_t b_i = 0, b_g = 0;                                    // slot B: position loaded
+    bool b_valid = false;
+    auto refill = [&]() {
+        const bool need = !b_valid;
+        const unsigned mask = __ballot_sync(0xffffffffu, need);
+        const int64_t idx = head + __popc(mask & below);
+        if (need && idx < end) {
+            b_i = idx;
+            b_g = pos[idx];
+            b_valid = true;
+        }
+        head += __popc(mask);
+    };
+
+    double2 a_anchor = make_double2(0.0, 0.0);                   // slot A: anchor load issued
+    int64_t a_i = 0;
+    int a_k = 0, a_off = 0;
+    bool a_valid = false, a_range = false;
+    auto promote = [&]() {                                       // A <- B
+        a_valid = b_valid;
+        a_i = b_i;
+        a_range = false;
+        if (b_valid) {
+            const int64_t g = b_g;
+            const int64_t q = g >= 0 ? g / T_cap : -1;
+            const int64_t tt = g - q * T_cap;
+            if (g < 0 || q >= n_streams || tt >= T) {
+                a_range = true;
+            } else {
+                const int64_t s = tt / t.L;
+                a_off = (int)(tt - s * t.L);
+                a_k = (int)min((int64_t)t.L, T - s * t.L) - 1;
+                a_anchor = anchors[q * S_cap + s];
+            }
+        }
+        b_valid = false;
+    };
+
+    double x = 0.0, y = 0.0;                                     // the current lookup
+    int64_t cur = 0;
+    int k = 0, off = 0;
+    bool bad = false, corrupt = false, range = false;
+    auto take = [&]() -> bool {                                  // current <- A; false if none
+        while (a_valid) {
+            cur = a_i;
+            if (a_range) {                                       // answered without a walk
+                out[cur] = kBad;
+                range = true;
+                promote();
+                continue;
+            }
+            x = a_anchor.x;
+            y = a_anchor.y;
+            k = a_k;
+            off = a_off;
+            bad = false;
+            promote();
+            return true;
+        }
+        return false;
+    };
+
+    refill();
+    promote();
+    refill();
+    bool has = take();
+    refill();
+    // Every round either moves some lane one step down its walk or hands out queued lookups, so the
+    // loop ends by itself; the cap only bounds it for the record.
+    const int cap = (per_warp + 4) * (kMaxSegment + 2);
+    for (int round = 0; round < cap && __any_sync(0xffffffffu, has || a_valid || b_valid); ++round) {
+        if (!has) {
+            if (!a_valid && b_valid) promote();
+            has = take();
+        }
+        if (has) {
+            double2 v;
+            int c = find_cell(x, y, t, v, bad);
+            bool step = k > off;
+            if (!step) {
+                out[cur] = bad ? kBad : (uint16_t)c;
+                corrupt |= bad;
+                has = take();
+                if (has) {
+                    c = find_cell(x, y, t, v, bad);
+                    step = k > off;
+                    if (!step) {
+                        out[cur] = bad ? kBad : (uint16_t)c;
+                        corrupt |= bad;
+                        has = false;
+                    }
+                }
+            }
+            if (step) {
+                backward_step(x, y, v, t.rinv);
+                --k;
+            }
+        }
+        refill();
     }
-    const int64_t s = tt / t.L;
-    const int off = (int)(tt - s * t.L);
-    const int len = (int)min((int64_t)t.L, T - s * t.L);
-    const double2 p = anchors[q * S_cap + s];
-    double x = p.x, y = p.y;
-    bool bad = false;
-    int c = 0;
-    for (int k = len - 1;; --k) {
-        double2 v;
-        c = find_cell(x, y, t, v, bad);
-        if (k <= off) break;
-        backward_step(x, y, v, t.rinv);
-    }
-    out[i] = bad ? kBad : (uint16_t)c;
-    if (bad) atomicOr(t.flags, (uint32_t)FA_FLAG_CORRUPT);
+    if (corrupt) atomicOr(t.flags, (uint32_t)FA_FLAG_CORRUPT);
+    if (range) atomicOr(t.flags, (uint32_t)FA_FLAG_RANGE);
 }
 
 struct DeviceGuard {
@@ -243,6 +369,7 @@ int fa_create(fa_ctx **out, int N, double r, int L, int device) {
 
     fa_ctx *c = new fa_ctx();
     c->device = device;
+    c->num_sms = prop.multiProcessorCount;
     c->N = N;
     c->L = L;
     c->r = r;
@@ -342,8 +469,14 @@ int fa_access(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_c
     if ((n + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
     DeviceGuard g(ctx->device);
     if (g.err != cudaSuccess) return FQ_ECUDA;
-    archive_access<<<blocks_for(n), kThreads, 0, (cudaStream_t)stream>>>(
-        tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, T_cap, S_cap, T, pos, n, out);
+    // Queue length per warp: enough warps for about kAccessWarpsPerSm per SM, 4 to 16 lookups per lane.
+    int64_t per_lane = (n + 32LL * ctx->num_sms * kAccessWarpsPerSm - 1) / (32LL * ctx->num_sms * kAccessWarpsPerSm);
+    per_lane = per_lane < kAccessMinPerLane ? kAccessMinPerLane : (per_lane > kAccessMaxPerLane ? kAccessMaxPerLane : per_lane);
+    const int per_warp = (int)(32 * per_lane);
+    const int64_t warps = (n + per_warp - 1) / per_warp;
+    archive_access<<<blocks_for(warps * 32), kThreads, 0, (cudaStream_t)stream>>>(
+        tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, T_cap, S_cap, T, pos, n, per_warp,
+        out);
     return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
 }
 

@@ -218,3 +218,37 @@ def test_full_size_workload_round_trip_and_sampled_oracle(name):
         else:
             np.testing.assert_allclose(got[q, s], want, rtol=0, atol=1e-15)
     ctx.close()
+
+
+def test_access_queue_with_uneven_walks_and_bad_positions():
+    """Lookups whose walks differ as much as possible, grouped so that some warps' lanes get only
+    zero-step lookups (the anchor's own symbol) and others only full walks, mixed with positions
+    outside the batch, repeats, and a count that is not a multiple of a warp's queue."""
+    N = 64
+    ctx, r, L = make(N)
+    nS, T_cap, T = 4, 1000, 997
+    sym = synth.symbol_streams(nS, T, N, sub=5)
+    A = fq.alloc_archive(ctx, nS, T_cap)
+    fq.fa_encode(ctx, to_dev(sym), nS, T, T_cap, 0, A)
+    rng = np.random.default_rng(2)
+    q = rng.integers(0, nS, size=3000)
+    seg = rng.integers(0, T // L, size=3000)
+    zero_step = q * T_cap + seg * L + L - 1                    # the anchor's own symbol
+    full_walk = q * T_cap + seg * L                             # L - 1 backward steps
+    mixed = synth.stream_positions(nS, T_cap, T, 3000, sub=3)
+    pos = np.concatenate([zero_step[:1024], full_walk[:1024], mixed, zero_step[1024:], full_walk[1024:2000]])
+    bad_at = np.arange(5, len(pos), 7)
+    pos[bad_at] = np.where(bad_at % 2, -3, nS * T_cap + 11)
+    pos[bad_at[::3]] = T_cap + T                                # position T of stream 1: past the end
+    pos = pos[:len(pos) - 13]
+    want = np.where(np.isin(np.arange(len(pos)), bad_at), 0xFFFF, 0).astype(np.uint16)
+    ok = want == 0
+    want[ok] = sym[pos[ok] // T_cap, pos[ok] % T_cap]
+    for n in (len(pos), 1, 31, 257):
+        acc = torch.empty(n, dtype=torch.int16, device="cuda")
+        fq.fa_access(ctx, A, nS, T_cap, T, torch.from_numpy(pos[:n].copy()).cuda(), n, acc)
+        torch.cuda.synchronize()
+        flags = fq.fa_status(ctx)
+        assert flags == (fq.FA_FLAG_RANGE if (~ok[:n]).any() else 0)
+        np.testing.assert_array_equal(to_host(acc), want[:n])
+    ctx.close()

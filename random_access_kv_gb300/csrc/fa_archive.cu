@@ -173,81 +173,87 @@ archive_decode(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
 //
 // A lookup needs between 0 and L - 1 backward steps, so one lookup per thread would leave most lanes
 // of a warp idle while the longest walk finishes, and every fp64 instruction costs the pipe the same
-// whatever its active lanes. Instead each warp owns a run of `per_warp` lookups as a queue: a lane
-// that answers its lookup takes the next one (its first decision in the same round), so the fp64
-// backward step of every round is shared by most lanes (about 3/4 of them with 8 lookups per lane,
-// 4/5 with 16, for walks of 0 .. 6 steps). Each lane keeps two lookups in flight behind the current
-// one: slot A with its anchor load issued, slot B with its position loaded; the queue hands out B
-// slots once per round through a warp ballot.
+// whatever its active lanes. Instead each warp owns a run of `per_warp` lookups as a queue:
+//   1. the warp turns every position of its run into (anchor index, walk length, target) in shared
+//      memory, all lanes together, so the integer divisions run convergent;
+//   2. a lane that answers its lookup takes the next one from the queue and makes that lookup's first
+//      decision in the same round, so the fp64 backward step of each round is shared by most lanes
+//      (about 3/4 of them with 8 lookups per lane, 4/5 with 16, for walks of 0 .. 6 steps);
+//   3. each lane keeps the next lookup's anchor load in flight (slot A) and holds the one after as a
+//      queue index (slot B); B slots are handed out once per round through a warp ballot.
 constexpr int kAccessMinPerLane = 4;
 constexpr int kAccessMaxPerLane = 16;
 constexpr int kAccessWarpsPerSm = 24;
+constexpr int kAccessOutOfRange = -1;
 
 __global__ void __launch_bounds__(kThreads)
 archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams, int64_t T_cap, int64_t S_cap,
                int64_t T, const int64_t *__restrict__ pos, int64_t n, int per_warp, uint16_t *__restrict__ out) {
-    const int lane = threadIdx.x & 31;
+    extern __shared__ __align__(16) unsigned char access_smem[];
+    const int lane = threadIdx.x & 31, warp_in_block = threadIdx.x >> 5;
     const int64_t begin = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * per_warp;
     if (begin >= n) return;                                      // uniform over the warp
-    const int64_t end = min(n, begin + per_warp);
-    const unsigned below = (1u << lane) - 1u;
-    int64_t head = begin;                                        // next unclaimed lookup (warp-uniform)
+    const int cnt = (int)min((int64_t)per_warp, n - begin);
+    int64_t *seg = reinterpret_cast<int64_t *>(access_smem) + (size_t)warp_in_block * per_warp;
+    uint16_t *walk = reinterpret_cast<uint16_t *>(reinterpret_cast<int64_t *>(access_smem) + (size_t)(kThreads / 32) * per_warp)
+                     + (size_t)warp_in_block * per_warp;
 
-    int64_t b_i = 0, b_g = 0;                                    // slot B: position loaded
-    bool b_valid = false;
-    auto refill = [&]() {
-        const bool need = !b_valid;
-        const unsigned mask = __ballot_sync(0xffffffffu, need);
-        const int64_t idx = head + __popc(mask & below);
-        if (need && idx < end) {
-            b_i = idx;
-            b_g = pos[idx];
-            b_valid = true;
+    // 1. positions -> (anchor index or kAccessOutOfRange, first position k | target off << 8)
+    for (int j = lane; j < cnt; j += 32) {
+        const int64_t g = pos[begin + j];
+        const int64_t q = g >= 0 ? g / T_cap : -1;
+        const int64_t tt = g - q * T_cap;
+        if (g < 0 || q >= n_streams || tt >= T) {
+            seg[j] = kAccessOutOfRange;
+            walk[j] = 0;
+        } else {
+            const int64_t s = tt / t.L;
+            seg[j] = q * S_cap + s;
+            walk[j] = (uint16_t)((min((int64_t)t.L, T - s * t.L) - 1) | ((tt - s * t.L) << 8));
         }
+    }
+    __syncwarp();
+
+    const unsigned below = (1u << lane) - 1u;
+    int head = 0;                                                // next unclaimed queue entry (warp-uniform)
+    int b = -1;                                                  // slot B: a queue entry, or -1
+    auto refill = [&]() {
+        const bool need = b < 0;
+        const unsigned mask = __ballot_sync(0xffffffffu, need);
+        const int idx = head + __popc(mask & below);
+        if (need && idx < cnt) b = idx;
         head += __popc(mask);
     };
 
-    double2 a_anchor = make_double2(0.0, 0.0);                   // slot A: anchor load issued
-    int64_t a_i = 0;
-    int a_k = 0, a_off = 0;
-    bool a_valid = false, a_range = false;
+    double2 a_anchor = make_double2(0.0, 0.0);                   // slot A: anchor load in flight
+    int a = -1;
+    int64_t a_seg = 0;
     auto promote = [&]() {                                       // A <- B
-        a_valid = b_valid;
-        a_i = b_i;
-        a_range = false;
-        if (b_valid) {
-            const int64_t g = b_g;
-            const int64_t q = g >= 0 ? g / T_cap : -1;
-            const int64_t tt = g - q * T_cap;
-            if (g < 0 || q >= n_streams || tt >= T) {
-                a_range = true;
-            } else {
-                const int64_t s = tt / t.L;
-                a_off = (int)(tt - s * t.L);
-                a_k = (int)min((int64_t)t.L, T - s * t.L) - 1;
-                a_anchor = anchors[q * S_cap + s];
-            }
+        a = b;
+        b = -1;
+        if (a >= 0) {
+            a_seg = seg[a];
+            if (a_seg != kAccessOutOfRange) a_anchor = anchors[a_seg];
         }
-        b_valid = false;
     };
 
     double x = 0.0, y = 0.0;                                     // the current lookup
-    int64_t cur = 0;
-    int k = 0, off = 0;
+    int cur = 0, k = 0, off = 0;
     bool bad = false, corrupt = false, range = false;
     auto take = [&]() -> bool {                                  // current <- A; false if none
-        while (a_valid) {
-            cur = a_i;
-            if (a_range) {                                       // answered without a walk
-                out[cur] = kBad;
+        while (a >= 0) {
+            cur = a;
+            if (a_seg == kAccessOutOfRange) {                    // answered without a walk
+                out[begin + cur] = kBad;
                 range = true;
                 promote();
                 continue;
             }
+            const int w = walk[cur];
             x = a_anchor.x;
             y = a_anchor.y;
-            k = a_k;
-            off = a_off;
+            k = w & 0xff;
+            off = w >> 8;
             bad = false;
             promote();
             return true;
@@ -263,9 +269,9 @@ archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
     // Every round either moves some lane one step down its walk or hands out queued lookups, so the
     // loop ends by itself; the cap only bounds it for the record.
     const int cap = (per_warp + 4) * (kMaxSegment + 2);
-    for (int round = 0; round < cap && __any_sync(0xffffffffu, has || a_valid || b_valid); ++round) {
+    for (int round = 0; round < cap && __any_sync(0xffffffffu, has || a >= 0 || b >= 0); ++round) {
         if (!has) {
-            if (!a_valid && b_valid) promote();
+            if (a < 0 && b >= 0) promote();
             has = take();
         }
         if (has) {
@@ -273,14 +279,14 @@ archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
             int c = find_cell(x, y, t, v, bad);
             bool step = k > off;
             if (!step) {
-                out[cur] = bad ? kBad : (uint16_t)c;
+                out[begin + cur] = bad ? kBad : (uint16_t)c;
                 corrupt |= bad;
                 has = take();
                 if (has) {
                     c = find_cell(x, y, t, v, bad);
                     step = k > off;
                     if (!step) {
-                        out[cur] = bad ? kBad : (uint16_t)c;
+                        out[begin + cur] = bad ? kBad : (uint16_t)c;
                         corrupt |= bad;
                         has = false;
                     }
@@ -474,7 +480,8 @@ int fa_access(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_c
     per_lane = per_lane < kAccessMinPerLane ? kAccessMinPerLane : (per_lane > kAccessMaxPerLane ? kAccessMaxPerLane : per_lane);
     const int per_warp = (int)(32 * per_lane);
     const int64_t warps = (n + per_warp - 1) / per_warp;
-    archive_access<<<blocks_for(warps * 32), kThreads, 0, (cudaStream_t)stream>>>(
+    const size_t smem = (size_t)(kThreads / 32) * per_warp * (sizeof(int64_t) + sizeof(uint16_t));
+    archive_access<<<blocks_for(warps * 32), kThreads, smem, (cudaStream_t)stream>>>(
         tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, T_cap, S_cap, T, pos, n, per_warp,
         out);
     return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;

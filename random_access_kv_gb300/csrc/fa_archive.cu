@@ -274,28 +274,30 @@ archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
             if (a < 0 && b >= 0) promote();
             has = take();
         }
-        if (has) {
-            double2 v;
-            int c = find_cell(x, y, t, v, bad);
-            bool step = k > off;
-            if (!step) {
+        double2 v = make_double2(0.0, 0.0);
+        int c = 0;
+        if (has) c = find_cell(x, y, t, v, bad);
+        bool again = false;
+        if (has && k <= off) {                                   // answered: take the next lookup
+            out[begin + cur] = bad ? kBad : (uint16_t)c;
+            corrupt |= bad;
+            has = take();
+            again = has;
+        }
+        if (again) {                                             // its first decision, this round
+            c = find_cell(x, y, t, v, bad);
+            if (k <= off) {
                 out[begin + cur] = bad ? kBad : (uint16_t)c;
                 corrupt |= bad;
-                has = take();
-                if (has) {
-                    c = find_cell(x, y, t, v, bad);
-                    step = k > off;
-                    if (!step) {
-                        out[begin + cur] = bad ? kBad : (uint16_t)c;
-                        corrupt |= bad;
-                        has = false;
-                    }
-                }
+                has = false;
             }
-            if (step) {
-                backward_step(x, y, v, t.rinv);
-                --k;
-            }
+        }
+        // One place for the fp64 step, reached by the whole warp, so its instructions are issued
+        // once per round for every lane that walks.
+        __syncwarp();
+        if (has && k > off) {
+            backward_step(x, y, v, t.rinv);
+            --k;
         }
         refill();
     }

@@ -176,9 +176,9 @@ archive_decode(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
 // whatever its active lanes. Instead each warp owns a run of `per_warp` lookups as a queue:
 //   1. the warp turns every position of its run into (anchor index, walk length, target) in shared
 //      memory, all lanes together, so the integer divisions run convergent;
-//   2. a lane that answers its lookup takes the next one from the queue and makes that lookup's first
-//      decision in the same round, so the fp64 backward step of each round is shared by most lanes
-//      (about 3/4 of them with 8 lookups per lane, 4/5 with 16, for walks of 0 .. 6 steps);
+//   2. a lane that answers its lookup takes the next one from the queue for the following round, so
+//      the fp64 backward step of each round is shared by most lanes (for walks of 0 .. 6 steps a lane
+//      walks in 3 of every 4 rounds, and the queue keeps about 4/5 of the lanes busy to the end);
 //   3. each lane keeps the next lookup's anchor load in flight (slot A) and holds the one after as a
 //      queue index (slot B); B slots are handed out once per round through a warp ballot.
 constexpr int kAccessMinPerLane = 4;
@@ -274,30 +274,17 @@ archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
             if (a < 0 && b >= 0) promote();
             has = take();
         }
-        double2 v = make_double2(0.0, 0.0);
-        int c = 0;
-        if (has) c = find_cell(x, y, t, v, bad);
-        bool again = false;
-        if (has && k <= off) {                                   // answered: take the next lookup
-            out[begin + cur] = bad ? kBad : (uint16_t)c;
-            corrupt |= bad;
-            has = take();
-            again = has;
-        }
-        if (again) {                                             // its first decision, this round
-            c = find_cell(x, y, t, v, bad);
-            if (k <= off) {
+        if (has) {
+            double2 v;
+            const int c = find_cell(x, y, t, v, bad);
+            if (k > off) {
+                backward_step(x, y, v, t.rinv);
+                --k;
+            } else {                                             // answered: the next lookup starts next round
                 out[begin + cur] = bad ? kBad : (uint16_t)c;
                 corrupt |= bad;
-                has = false;
+                has = take();
             }
-        }
-        // One place for the fp64 step, reached by the whole warp, so its instructions are issued
-        // once per round for every lane that walks.
-        __syncwarp();
-        if (has && k > off) {
-            backward_step(x, y, v, t.rinv);
-            --k;
         }
         refill();
     }

@@ -109,7 +109,9 @@ def measured_peaks() -> dict:
 # traffic figure to the code it measured.
 KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu"],
                   "encode_full_tc": ["fq_encode_full_tc.cu"], "decode_tc": ["fq_decode_tc.cu"],
-                  "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"]}
+                  "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"],
+                  "archive_encode": ["fa_archive.cu"], "archive_decode": ["fa_archive.cu"],
+                  "archive_access": ["fa_archive.cu"]}
 
 
 def source_hash(kernel: str) -> str:
@@ -130,11 +132,13 @@ def kernel_of(w, op: str) -> str:
     return "decode_full" if w.k == w.d else "decode_tc"
 
 
-def committed_traffic(kernel: str, workload: int, rows_per_launch: int):
-    """DRAM bytes per launch from profiles/<kernel>_w<workload>.md, if that capture was taken on the
-    kernel's current sources; a capture of a smaller case is scaled by rows (traffic grows in
-    proportion to the rows a launch processes)."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_w{workload}.md")
+def committed_traffic(kernel: str, workload, rows_per_launch: int):
+    """DRAM bytes per launch from profiles/<kernel>_w<workload>.md (profiles/<kernel>_<workload>.md
+    for a named workload), if that capture was taken on the kernel's current sources; a capture of
+    a smaller case is scaled by rows (traffic grows in proportion to the rows, symbols or lookups a
+    launch processes)."""
+    stem = f"{kernel}_w{workload}" if isinstance(workload, int) else f"{kernel}_{workload}"
+    p = os.path.join(ROOT, "profiles", stem + ".md")
     if not os.path.exists(p):
         return None
     vals = {}
@@ -975,7 +979,9 @@ def run_archive(args) -> None:
     peaks = measured_peaks()
     peak = peaks["sms"] * FA_FP64_PER_SM_CLK * sm_mhz * 1e6 / 1e12     # T fp64 instructions / s
     ach = {k: fp64[k] / (times[k] / 1e3) / 1e12 for k in times}
-    roofline = {"kernel": dom, "cuda_kernel": "archive_" + dom, "traffic": None, "bound": "alu",
+    units = {"encode": nS * T, "decode": nS * T, "access": w.lookups}
+    traffic = committed_traffic("archive_" + dom, "kv-streams", units[dom])
+    roofline = {"kernel": dom, "cuda_kernel": "archive_" + dom, "traffic": traffic, "bound": "alu",
                 "achieved": round(ach[dom], 4), "peak": round(peak, 4), "unit": "T fp64 instr/s",
                 "frac": round(ach[dom] / peak, 4), "peak_source": "nominal fp64 rate (2 per SM per clock) at the "
                 "sampled SM clock", "fp64_instr_per_launch": fp64[dom], "launch_ms": round(times[dom], 5),

@@ -58,9 +58,9 @@ import synth  # noqa: E402
 METRIC = "KV vectors/s encoded and decoded (fp16 GB/s) per bitrate; % of HBM/TC roofline"
 ATTEND_METRIC = "cached KV vectors/s attended (fused decode-into-attention)"
 ARCHIVE_METRIC = "archive symbols/s (encode + decode round trip, with a batch of random accesses)"
-# fp64 arithmetic instructions the archive kernels issue: a forward step is a subtract, a multiply
-# and an add per coordinate; a backward step a subtract and a fused multiply-add per coordinate.
-FA_FWD_FP64, FA_BWD_FP64 = 6, 4
+# fp64 arithmetic instructions the archive kernels issue: a forward or a backward step is a
+# subtract and a fused multiply-add per coordinate.
+FA_FWD_FP64, FA_BWD_FP64 = 4, 4
 # fp64 instructions per SM per clock: the nominal 1.25 TFLOP/s of GB300 over 2 flops per fused
 # multiply-add, 152 SMs and the 2070 MHz maximum clock.
 FA_FP64_PER_SM_CLK = 2.0

@@ -13,8 +13,9 @@
  *       and a segment is rebuilt from its anchor by a backward search: the symbol is the cell that
  *       holds the point, then that symbol's map is inverted.
  * Readings of what the page leaves open: every segment starts at the origin (segments are
- * independent); forward steps are computed in fp64 as t = p - V, t = r t, p = V + t per coordinate
- * with every operation rounded, so anchors do not depend on how segments are split across calls.
+ * independent); forward steps are computed in fp64 per coordinate as t = p - V, p = r t + V (one
+ * fused multiply-add), always in that order, so anchors do not depend on how segments are split
+ * across calls.
  *
  * Layout. A batch of n_streams streams of capacity T_cap symbols keeps S_cap = ceil(T_cap / L)
  * anchors per stream: anchors is double [n_streams][S_cap][2] (x, y), 16-byte aligned, stream q's
@@ -54,7 +55,8 @@ double fa_ratio_limit(int N);
 /*
  * fa_max_segment - the longest segment whose backward search is exact in fp64 for (N, r), capped
  * at 64; 0 if r is not in (0, fa_ratio_limit(N)) or not one symbol fits.
- * Bound used: a forward step's rounding error per coordinate is below 1.01 u (1 + 4 r) and a
+ * Bound used: a forward step's rounding error per coordinate is below 1.01 u (1 + 4 r) (that of a
+ * rounded product and a rounded sum; the fused form this library uses errs less) and a
  * backward step's below 8 u (u = 2^-53); the error of the rebuilt point grows by 1/r per backward
  * step, and all L decisions of a segment are correct when it stays below half the margin
  * (1 - r) sin(pi/N) - r between a cell and the edges of its angular sector.

@@ -5,9 +5,10 @@
 // segment (encode, decode) or one lookup (random access). The work is a chain of dependent fp64
 // steps per thread: GB300 runs fp64 at a small fraction of its fp32 rate, so these kernels are
 // bound by the fp64 pipe, not by memory (2 bytes per symbol in, 16 bytes per segment out).
-//   * forward step, per coordinate: t = p - V, t = r t, p = V + t, each operation rounded (no
-//     contraction into a fused multiply-add), which makes anchors identical whatever the split of a
-//     stream into append calls;
+//   * forward step, per coordinate: t = p - V, then p = r t + V as one fused multiply-add (two fp64
+//     instructions, one rounding fewer than the three-operation form, so the error bound behind
+//     the segment length still holds); a fixed instruction sequence makes anchors identical
+//     whatever the split of a stream into append calls;
 //   * backward step: the cell is found in fp32 (the angle of the point rounded to the nearest
 //     vertex; the cells are disjoint with a margin the context guarantees to be at least 2e-5, far
 //     above fp32 error), the point is checked to lie within r + 3/4 of the margin of that cell's
@@ -63,8 +64,8 @@ Tables tables_of(const fa_ctx *c) {
 }
 
 __device__ __forceinline__ void forward_step(double &x, double &y, double2 v, double r) {
-    x = __dadd_rn(v.x, __dmul_rn(r, __dsub_rn(x, v.x)));
-    y = __dadd_rn(v.y, __dmul_rn(r, __dsub_rn(y, v.y)));
+    x = __fma_rn(r, __dsub_rn(x, v.x), v.x);
+    y = __fma_rn(r, __dsub_rn(y, v.y), v.y);
 }
 
 __device__ __forceinline__ void backward_step(double &x, double &y, double2 v, double rinv) {

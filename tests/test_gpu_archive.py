@@ -35,14 +35,16 @@ def make(N, rho=0.75, L=None):
     return fq.fa_create(N, r, L), r, L
 
 
+# Anchors: the library forms p = r (p - V) + V with one fused multiply-add, the oracle with a
+# rounded product and a rounded sum. Per step and coordinate the two differ by at most
+# delta_lib + delta_orc <= u (1 + 2r) + 1.01 u (1 + 4r) < 5.1 u (|p| <= 1, |p - V| <= 2, r < 1/2),
+# and a difference made k steps before the end is scaled by r^k, so the sum over a segment is below
+# 5.1 u / (1 - r) <= 10.2 u; one-ulp differences between the two vertex tables add at most u.
+ANCHOR_TOL = 12 * 2.0 ** -53
+
+
 def check_anchors(ctx, got, want):
-    """Bit-exact when the library's vertex table equals the oracle's bit for bit (the same fp64
-    operations in the same order); otherwise within what one-ulp differences of V can move a point."""
-    N, _, _ = fq.fa_params(ctx)
-    if np.array_equal(fq.fa_vertex_table(ctx), ofa.vertices(N)):
-        np.testing.assert_array_equal(got, want)
-    else:
-        np.testing.assert_allclose(got, want, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(got, want, rtol=0, atol=ANCHOR_TOL)
 
 
 def test_vertex_table_within_one_ulp_of_the_oracle():
@@ -210,13 +212,9 @@ def test_full_size_workload_round_trip_and_sampled_oracle(name):
     S = got.shape[1]
     rng = np.random.default_rng(7)
     V = ofa.vertices(w.N)
-    exact = np.array_equal(fq.fa_vertex_table(ctx), V)
     for q, s in zip(rng.integers(0, w.n_streams, 400), rng.integers(0, S, 400)):
         want = ofa.encode_segment(sym[q, s * L:min(s * L + L, w.T)], w.N, r, V=V)
-        if exact:
-            assert tuple(got[q, s]) == want
-        else:
-            np.testing.assert_allclose(got[q, s], want, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(got[q, s], want, rtol=0, atol=ANCHOR_TOL)
     ctx.close()
 
 

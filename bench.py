@@ -379,7 +379,8 @@ def run_ours(args) -> None:
 
         def arrival_order(a):  # [n_seq*T, d] -> [steps, n_seq, new, d], the order tokens arrive in
             return np.ascontiguousarray(a.reshape(n_seq, n_steps, new, d).transpose(1, 0, 2, 3))
-        x_np = np.concatenate([arrival_order(synth.kv_tensor(cfg, t, rows=M)) for t in range(nt)], axis=1)
+        x_np = np.concatenate([arrival_order(synth.kv_tensor(cfg, t, rows=M if M < w.rows else None))
+                               for t in range(nt)], axis=1)
         x_np = x_np.reshape(n_steps, nt * n_seq * new, d)
     else:
         x_np = np.concatenate([synth.kv_tensor(cfg, t, rows=M) for t in range(nt)])

@@ -1031,6 +1031,11 @@ SWEEP_POINTS = ([("scalar", 1, n) for n in (2, 4, 8, 16)]
                 + [("fibquant", 4, n) for n in (16, 64, 256, 1024, 4096)]
                 + [("fibquant", 8, n) for n in (256, 4096)]
                 + [("fibquant", 64, n) for n in (256, 1024, 4096)])
+# d = 96 (a head dimension that 3 divides): integer rates 1, 2, 3 for k = 1, 2, 3 (Fibonacci sphere), 4.
+SWEEP_POINTS_96 = ([("scalar", 1, n) for n in (2, 4, 8)]
+                   + [("fibquant", 2, n) for n in (4, 16, 64)]
+                   + [("fibquant", 3, n) for n in (8, 64, 512)]
+                   + [("fibquant", 4, n) for n in (16, 256, 4096)])
 
 
 def run_rate_sweep(args) -> None:
@@ -1047,7 +1052,8 @@ def run_rate_sweep(args) -> None:
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     fbuild.build()
-    d, rows, seed = 64, args.rows or 262144, 1
+    d, rows, seed = args.sweep_d, args.rows or 262144, 1
+    sweep = SWEEP_POINTS if d == 64 else SWEEP_POINTS_96
     Pi = pcb.haar(synth.rotation_gaussian(seed, d)).astype(np.float32)
     x_np = synth.gaussian_rows(seed, 3, rows, d)
     x = torch.from_numpy(x_np).to(dev)
@@ -1057,12 +1063,12 @@ def run_rate_sweep(args) -> None:
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     points = []
-    for i, (codec, k, N) in enumerate(SWEEP_POINTS):
+    for i, (codec, k, N) in enumerate(sweep):
         t0 = time.perf_counter()
         if codec == "scalar":
             C, _ = pcb.scalar_lloyd_max(d, N)
         else:
-            kind = "sphere" if k == d else ("spiral" if k == 2 else "kronecker")
+            kind = "sphere" if k == d else {2: "spiral", 3: "fibsphere"}.get(k, "kronecker")
             T = int(min(131072, max(32768, 32 * N)))
             C, _ = pcb.build(kind, d, k, N, synth.source_gaussians(seed, T, d, chunk=100 + i), 10)
         build_s = time.perf_counter() - t0
@@ -1176,6 +1182,8 @@ def main():
     ap.add_argument("--attend", action="store_true", help="time fused decode-into-attention")
     ap.add_argument("--rate-sweep", action="store_true",
                     help="relative MSE and throughput against bits per coordinate (scalar k = 1 vs FibQuant)")
+    ap.add_argument("--sweep-d", type=int, choices=[64, 96], default=64,
+                    help="with --rate-sweep: the head dimension (96 adds the k = 3 Fibonacci-sphere code)")
     ap.add_argument("--lloyd", action="store_true",
                     help="codebook building: host numpy Lloyd against the GPU Lloyd for --workload")
     ap.add_argument("--q-per-group", type=int, default=1,

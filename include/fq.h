@@ -62,7 +62,9 @@ enum {
  * fq_codebook_load - build a context holding the shared codebook and rotation on `device`.
  *   C_host  : host float32 [N x k], row n = codeword c_n [FibQuant §2.2]. Copied.
  *   N       : codebook size, a power of two, 2 <= N <= 65536.
- *   k       : block size. Supported: k in {1, 2, 4, 8} with d in {64, 128}, and k = d = 64.
+ *   k       : block size. Supported: k in {1, 2, 4, 8} with d in {64, 128}; k in {1, 2, 3, 4, 8}
+ *             with d = 96 (CUDA-core kernels only; k = 3 takes the Fibonacci-sphere codebook of
+ *             [FibQuant §2.2]); and k = d = 64.
  *   Pi_host : host float32 [d x d], row-major, the shared rotation u = Pi x [FibQuant §2.1].
  *             Used as given (orthogonality is the caller's business). Copied.
  *   d       : vector dimension (head dim).
@@ -143,8 +145,9 @@ int fq_decode_gather_f32(fq_ctx *ctx, const float *nu, const uint32_t *codes, in
  *                 such row must lie in [0, M) (else FQ_EINVAL);
  *   scale       : finite score scale (commonly 1/sqrt(d));
  *   out         : device float32 [n_queries x d].
- * Non-finite norms in the store give non-finite outputs. Returns FQ_EINVAL when the codebook and
- * record staging of this context do not fit one CTA's shared memory.
+ * Non-finite norms in the store give non-finite outputs. Returns FQ_EINVAL for d = 96 contexts
+ * (no attention kernel) and when the codebook and record staging of this context do not fit one
+ * CTA's shared memory.
  */
 int fq_attend(fq_ctx *ctx, const float *nu, const uint32_t *codes, int64_t M, const void *q,
               int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,

@@ -12,7 +12,12 @@ Readings of the page where it is open:
     Beta(k/2, a+1), a = k (d-k-2) / (2 (k+2)); r_n = sqrt(BetaQuantile((n + 1/2) / N)).
     For k = 2 this is the closed form r_n = sqrt(1 - (1 - (n+1/2)/N)^(4/d)).
   * k = 2 directions: planar Fibonacci spiral, angle n * 2 pi (1 - 1/phi), paired with r_n.
-  * k >= 3 directions: Roberts-Kronecker points t_n = frac(s + (n+1) alpha), alpha_j = phi_k^-j
+  * k = 3 directions: the Fibonacci sphere, point j at height z_j = 1 - (2j + 1)/N and azimuth j times
+    the golden angle. Its points are ordered by height, so radius n (also ordered) takes point
+    j = (n m) mod N, m the odd integer nearest N / phi coprime to N (a golden-ratio stride), which
+    spreads consecutive radii over the sphere as the k = 2 spiral's golden angle spreads them
+    over the circle.
+  * k >= 4 directions: Roberts-Kronecker points t_n = frac(s + (n+1) alpha), alpha_j = phi_k^-j
     (j = 1..k, phi_k the real root > 1 of x^(k+1) = x + 1; the sequence starts at its first
     term, so that codeword 0 is not the centre point t = s), mapped to the sphere by the inverse
     normal CDF and normalisation; codeword n = r_n u_n. For k = d the codewords are the unit
@@ -69,6 +74,35 @@ def spiral_codebook(d: int, N: int) -> np.ndarray:
     return np.stack([r * np.cos(theta), r * np.sin(theta)], axis=1)
 
 
+def fibonacci_sphere(N: int) -> np.ndarray:
+    """k = 3 directions [FibQuant §2.2, 'Fibonacci sphere']: point j at height z_j = 1 - (2j+1)/N,
+    the centres of N slabs of equal height and hence (Archimedes' hat-box theorem) equal area, and
+    azimuth j times the golden angle 2 pi (1 - 1/phi)."""
+    j = np.arange(N, dtype=np.float64)
+    z = 1.0 - (2.0 * j + 1.0) / N
+    theta = j * (2.0 * np.pi * (1.0 - 1.0 / GOLDEN_RATIO))
+    rho = np.sqrt(1.0 - z * z)
+    return np.stack([rho * np.cos(theta), rho * np.sin(theta), z], axis=1)
+
+
+def golden_stride(N: int) -> int:
+    """The integer nearest N / phi that is coprime to N (the nearer below on a tie)."""
+    target = N / GOLDEN_RATIO
+    best = None
+    for m in range(1, N + 1):
+        if np.gcd(m, N) == 1 and (best is None or abs(m - target) < abs(best - target)):
+            best = m
+    return best
+
+
+def fibsphere_codebook(d: int, N: int) -> np.ndarray:
+    """k = 3 radial-angular initialisation: codeword n = r_n u_{(n m) mod N} with the companded
+    radii r_n and the Fibonacci sphere u [FibQuant §2.2]."""
+    r = companded_radii(d, 3, N)
+    u = fibonacci_sphere(N)
+    return r[:, None] * u[(np.arange(N) * golden_stride(N)) % N]
+
+
 def roberts_root(k: int) -> float:
     """phi_k: the real root > 1 of x^(k+1) = x + 1, by bisection on [1, 2]."""
     lo, hi = 1.0, 2.0
@@ -98,6 +132,10 @@ def initial_codebook(kind: str, d: int, k: int, N: int, s: float = 0.5) -> np.nd
         if k != 2:
             raise ValueError("spiral codebook is k = 2")
         return spiral_codebook(d, N)
+    if kind == "fibsphere":
+        if k != 3:
+            raise ValueError("Fibonacci-sphere codebook is k = 3")
+        return fibsphere_codebook(d, N)
     u = kronecker_directions(N, k, s)
     if kind == "sphere":
         if k != d:

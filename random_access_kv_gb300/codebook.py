@@ -8,7 +8,10 @@ vector quantisation for random-access KV-cache compression":
   radii     Bennett-Gersho companding of the spherical-Beta block law: the point density
             ~ f^(k/(k+2)) makes t = rho^2 of the codewords Beta(k/2, 1 + k(d-k-2)/(2(k+2)));
             r_n is the square root of that law's quantile at (n + 1/2)/N.
-  angles    k = 2: Fibonacci spiral (golden angle per index). k >= 3: Roberts-Kronecker points
+  angles    k = 2: Fibonacci spiral (golden angle per index). k = 3 ("fibsphere"): the Fibonacci
+            sphere (heights at the centres of N equal slabs, golden-angle azimuths), visited with
+            a golden-ratio stride m ~ N / phi coprime to N so that consecutive radii land far
+            apart on the sphere. k >= 4: Roberts-Kronecker points
             frac(s + (n+1) phi_k^-j), j = 1..k, pushed through the inverse normal CDF and
             normalised; phi_k solves x^(k+1) = x + 1. k = d: the unit directions alone.
   Lloyd     multi-restart Lloyd on draws of the block source (first k coordinates of a Gaussian
@@ -64,7 +67,25 @@ def directions(N: int, k: int, s: float) -> np.ndarray:
     return z / np.linalg.norm(z, axis=1, keepdims=True)
 
 
+def fibonacci_sphere(N: int) -> np.ndarray:
+    z = np.linspace(1.0 - 1.0 / N, -1.0 + 1.0 / N, N)
+    a = np.pi * (3.0 - np.sqrt(5.0)) * np.arange(N, dtype=np.float64)
+    ring = np.sqrt(np.maximum(0.0, 1.0 - z * z))
+    return np.column_stack([ring * np.cos(a), ring * np.sin(a), z])
+
+
+def _golden_stride(N: int) -> int:
+    target = N * (np.sqrt(5.0) - 1.0) / 2.0        # N / phi
+    cands = [m for m in range(1, N + 1) if np.gcd(m, N) == 1]
+    return min(cands, key=lambda m: (abs(m - target), m))
+
+
 def initial(kind: str, d: int, k: int, N: int, s: float = 0.5) -> np.ndarray:
+    if kind == "fibsphere":
+        if k != 3:
+            raise ValueError("the Fibonacci-sphere codebook is for k = 3")
+        order = (np.arange(N) * _golden_stride(N)) % N
+        return radii(d, 3, N)[:, None] * fibonacci_sphere(N)[order]
     u = directions(N, k, s)
     if kind == "sphere":
         return u

@@ -90,8 +90,9 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     if (!C_host || !Pi_host) return FQ_EINVAL;
     const int B = log2_exact(N);
     if (B < 0 || N > 65536) return FQ_EINVAL;
-    const bool blocks_ok = (d == 64 || d == 128) && (k == 1 || k == 2 || k == 4 || k == 8) &&
-                           (size_t)N * k <= 32768;
+    // Block codes: d = 64 and 128 (all paths), d = 96 (CUDA-core kernels; k = 3 lives here).
+    const bool blocks_ok = (d == 64 || d == 96 || d == 128) && (k == 1 || k == 2 || k == 3 || k == 4 || k == 8) &&
+                           d % k == 0 && (size_t)N * k <= 32768;
     const bool full_ok = (d == 64 && k == 64 && N >= 64);
     if (!blocks_ok && !full_ok) return FQ_EINVAL;
     for (size_t i = 0; i < (size_t)N * k; ++i)

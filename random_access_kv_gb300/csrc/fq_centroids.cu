@@ -123,6 +123,12 @@ cudaError_t launch_centroid_sums(const fq_ctx *ctx, const __half *x, int64_t M, 
         if (ctx->k == 4) return CALL(64, 4);
         if (ctx->k == 8) return CALL(64, 8);
         if (ctx->k == 64) return CALL(64, 64);
+    } else if (ctx->d == 96) {
+        if (ctx->k == 1) return CALL(96, 1);
+        if (ctx->k == 2) return CALL(96, 2);
+        if (ctx->k == 3) return CALL(96, 3);
+        if (ctx->k == 4) return CALL(96, 4);
+        if (ctx->k == 8) return CALL(96, 8);
     } else if (ctx->d == 128) {
         if (ctx->k == 1) return CALL(128, 1);
         if (ctx->k == 2) return CALL(128, 2);

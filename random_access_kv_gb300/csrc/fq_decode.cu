@@ -114,6 +114,12 @@ cudaError_t launch_decode_blocks(const fq_ctx *ctx, const float *nu, const uint3
         if (ctx->k == 2) return CALL(64, 2);
         if (ctx->k == 4) return CALL(64, 4);
         if (ctx->k == 8) return CALL(64, 8);
+    } else if (ctx->d == 96) {
+        if (ctx->k == 1) return CALL(96, 1);
+        if (ctx->k == 2) return CALL(96, 2);
+        if (ctx->k == 3) return CALL(96, 3);
+        if (ctx->k == 4) return CALL(96, 4);
+        if (ctx->k == 8) return CALL(96, 8);
     } else if (ctx->d == 128) {
         if (ctx->k == 1) return CALL(128, 1);
         if (ctx->k == 2) return CALL(128, 2);
@@ -131,6 +137,12 @@ cudaError_t prepare_decode_blocks(const fq_ctx *ctx) {
         if (ctx->k == 2) return CALL(64, 2);
         if (ctx->k == 4) return CALL(64, 4);
         if (ctx->k == 8) return CALL(64, 8);
+    } else if (ctx->d == 96) {
+        if (ctx->k == 1) return CALL(96, 1);
+        if (ctx->k == 2) return CALL(96, 2);
+        if (ctx->k == 3) return CALL(96, 3);
+        if (ctx->k == 4) return CALL(96, 4);
+        if (ctx->k == 8) return CALL(96, 8);
     } else if (ctx->d == 128) {
         if (ctx->k == 1) return CALL(128, 1);
         if (ctx->k == 2) return CALL(128, 2);

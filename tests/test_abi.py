@@ -48,7 +48,7 @@ def _load(L, C, Pi):
     return rc, h.value
 
 
-@pytest.mark.parametrize("N,k,d", [(12, 2, 64), (1, 2, 64), (256, 3, 64), (256, 2, 96), (131072, 2, 64),
+@pytest.mark.parametrize("N,k,d", [(12, 2, 64), (1, 2, 64), (256, 3, 64), (256, 2, 80), (256, 3, 128), (131072, 2, 64),
                                    (65536, 2, 64), (16, 64, 64), (256, 128, 128)])
 def test_codebook_load_rejects_unsupported_shapes(L, N, k, d):
     rc, h = _load(L, np.zeros((N, k)), np.eye(d))
@@ -103,3 +103,17 @@ def test_archive_limits_match_the_oracle(L):
             r = rho * ofa.ratio_limit(N)
             assert L.fa_max_segment(N, r) == ofa.max_segment(N, r), (N, rho)
     assert L.fa_ratio_limit(1) == 0.0 and L.fa_max_segment(1, 0.1) == 0 and L.fa_max_segment(8, -0.1) == 0
+
+
+def test_codebook_load_accepts_k3_at_d96(L):
+    # d = 96 with k = 3 (the Fibonacci-sphere codebook) passes the shape checks; without a GPU
+    # the load then stops at the device check. k = 3 with d = 64 or 128 does not divide d.
+    rc, h = _load(L, np.zeros((64, 3)), np.eye(96))
+    assert rc in (fb.FQ_ENODEV, fb.FQ_OK) and (rc != fb.FQ_OK or h)
+    if h:
+        L.fq_destroy(ctypes.c_void_p(h))
+    for d in (64, 128):
+        rc, h = _load(L, np.zeros((64, 3)), np.eye(d))
+        assert rc == fb.FQ_EINVAL and not h
+    rc, h = _load(L, np.zeros((64, 5)), np.eye(96))
+    assert rc == fb.FQ_EINVAL

@@ -16,7 +16,8 @@ def test_builder_matches_oracle(cfg):
 
 
 @pytest.mark.parametrize("d,k,N,kind", [(64, 4, 1024, "kronecker"), (128, 8, 4096, "kronecker"),
-                                        (64, 64, 256, "sphere"), (64, 2, 64, "spiral")])
+                                        (64, 64, 256, "sphere"), (64, 2, 64, "spiral"),
+                                        (96, 3, 8, "fibsphere"), (96, 3, 512, "fibsphere")])
 def test_initialisation_matches_oracle(d, k, N, kind):
     s = 0.5 if kind != "sphere" else 0.3
     np.testing.assert_allclose(pcb.initial(kind, d, k, N, s), ocb.initial_codebook(kind, d, k, N, s),
@@ -24,5 +25,5 @@ def test_initialisation_matches_oracle(d, k, N, kind):
 
 
 def test_radii_agree_for_every_k():
-    for d, k, N in [(64, 2, 256), (64, 4, 1024), (128, 8, 4096), (64, 1, 16)]:
+    for d, k, N in [(64, 2, 256), (64, 4, 1024), (128, 8, 4096), (64, 1, 16), (96, 3, 512)]:
         np.testing.assert_allclose(pcb.radii(d, k, N), ocb.companded_radii(d, k, N), rtol=1e-10)

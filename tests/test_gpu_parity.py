@@ -152,6 +152,8 @@ def _small_codebook(d, k, N, seed):
     Pi = ocb.haar_rotation(r.standard_normal((d, d))).astype(np.float32)
     if k == d:
         C = ocb.kronecker_directions(N, k, 0.37) * r.uniform(0.5, 1.0, size=(N, 1))
+    elif k == 3:
+        C = ocb.initial_codebook("fibsphere", d, 3, N)
     else:
         C = ocb.companded_radii(d, k, N)[:, None] * ocb.kronecker_directions(N, k, 0.5) if k >= 3 else \
             (ocb.spiral_codebook(d, N) if k == 2 else np.sort(r.standard_normal((N, 1)) * 0.2, axis=0))
@@ -161,7 +163,9 @@ def _small_codebook(d, k, N, seed):
 @pytest.mark.parametrize("d,k,N", [(64, 4, 8), (64, 8, 2), (64, 2, 2), (128, 1, 8), (64, 64, 128),
                                    (128, 4, 64), (64, 1, 16), (64, 4, 256), (128, 8, 128), (64, 8, 512),
                                    (128, 4, 1024), (128, 2, 64), (64, 2, 128), (64, 1, 2), (128, 1, 4),
-                                   (128, 2, 256), (64, 8, 4096), (128, 8, 4096)])
+                                   (128, 2, 256), (64, 8, 4096), (128, 8, 4096),
+                                   (96, 3, 8), (96, 3, 64), (96, 3, 512), (96, 3, 4096), (96, 1, 4),
+                                   (96, 2, 16), (96, 4, 256), (96, 8, 128)])
 @pytest.mark.parametrize("row0", [0, 1, 7, 45])
 def test_records_at_any_bit_offset_preserve_neighbours(d, k, N, row0):
     C, Pi = _small_codebook(d, k, N, d * 1000 + k * 10 + N)

@@ -32,7 +32,8 @@ def codebook(kind, d, k, N):
 
 @pytest.mark.parametrize("kind,d,k,N", [("scalar", 64, 1, 2), ("scalar", 64, 1, 16), ("scalar", 128, 1, 8),
                                         ("spiral", 64, 2, 32), ("spiral", 64, 2, 128),
-                                        ("kronecker", 64, 4, 1024), ("kronecker", 128, 8, 256)],
+                                        ("kronecker", 64, 4, 1024), ("kronecker", 128, 8, 256),
+                                        ("fibsphere", 96, 3, 64), ("fibsphere", 96, 3, 512), ("scalar", 96, 1, 4)],
                          ids=lambda v: str(v))
 def test_rate_point_parity_and_mse(kind, d, k, N):
     C = codebook(kind, d, k, N)

@@ -120,3 +120,52 @@ def test_workload_codebooks_shapes_and_restart_choice():
         assert np.unique(C, axis=0).shape[0] == w.N
     Pi = ow.rotation(2)
     assert Pi.dtype == np.float32 and Pi.shape == (64, 64)
+
+
+def test_fibonacci_sphere_equal_area_and_golden_azimuth():
+    # k = 3 directions (section 2.2, Fibonacci sphere). Heights are the centres of N equal slabs,
+    # so by Archimedes' hat-box theorem every cap z > z0 holds its area's share of points to within
+    # one point; consecutive azimuths differ by the golden angle; spacing is ~3.09 / sqrt(N).
+    for N in (16, 64, 512, 2048):
+        u = ocb.fibonacci_sphere(N)
+        np.testing.assert_allclose(np.linalg.norm(u, axis=1), 1.0, atol=1e-14)
+        np.testing.assert_allclose(np.sort(u[:, 2]), -1.0 + (2.0 * np.arange(N) + 1.0) / N, atol=1e-14)
+        for z0 in np.linspace(-0.95, 0.95, 13):
+            assert abs(np.sum(u[:, 2] > z0) - N * (1.0 - z0) / 2.0) <= 1.0
+        az = np.arctan2(u[:, 1], u[:, 0])
+        step = np.mod(np.diff(az), 2 * np.pi)
+        np.testing.assert_allclose(step, np.pi * (3.0 - np.sqrt(5.0)), atol=1e-9)
+        D = np.linalg.norm(u[:, None] - u[None], axis=2)
+        np.fill_diagonal(D, 9.0)
+        assert D.min() * np.sqrt(N) > 3.0
+
+
+def test_fibsphere_codebook_pairs_radii_and_directions():
+    d = 96
+    for N in (8, 64, 512):
+        C = ocb.initial_codebook("fibsphere", d, 3, N)
+        r = np.linalg.norm(C, axis=1)
+        np.testing.assert_allclose(r, ocb.companded_radii(d, 3, N), rtol=1e-13)
+        u = C / r[:, None]
+        S = ocb.fibonacci_sphere(N)
+        # the directions are the Fibonacci sphere's, each used once
+        match = np.argmin(np.linalg.norm(u[:, None] - S[None], axis=2), axis=1)
+        assert np.array_equal(np.sort(match), np.arange(N))
+        m = ocb.golden_stride(N)
+        assert np.gcd(m, N) == 1 and abs(m - N / ocb.GOLDEN_RATIO) < 2
+        if N >= 64:
+            # the stride decorrelates radius from height (pairing in order would give about -1)
+            assert abs(np.corrcoef(r, u[:, 2])[0, 1]) < 0.2
+    with pytest.raises(ValueError):
+        ocb.initial_codebook("fibsphere", 96, 2, 16)
+
+
+def test_k3_vector_beats_scalar_at_matched_rate():
+    # b = 2 bits per coordinate at d = 96: the k = 3, N = 64 Fibonacci-sphere code refined by Lloyd
+    # has lower MSE per coordinate than the scalar (k = 1, N = 4) Lloyd-Max quantiser.
+    g = np.random.default_rng(12).standard_normal((60000, 96))
+    Y = ocb.source_points(g, 3)
+    C3, h3 = ocb.lloyd(ocb.initial_codebook("fibsphere", 96, 3, 64), Y, 30)
+    y1 = Y[:, :1]
+    C1, h1 = ocb.lloyd(np.quantile(y1, [0.125, 0.375, 0.625, 0.875])[:, None], y1, 60)
+    assert h3[-1] / 3 < h1[-1]

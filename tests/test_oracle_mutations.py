@@ -138,3 +138,11 @@ def test_optimistic_segment_bound_is_caught(monkeypatch):
     orig = ofa.max_segment
     monkeypatch.setattr(ofa, "max_segment", lambda N, r, cap=64: 3 * orig(N, r, cap))
     assert _fails(tf.test_round_trip_at_the_segment_limit, 256)
+
+
+def test_in_order_radius_pairing_is_caught(monkeypatch):
+    # pairing the n-th radius with the n-th (height-ordered) sphere point ties radius to height
+    from oracle import codebook as ocb2
+    import test_oracle_codebook as tcb
+    monkeypatch.setattr(ocb2, "golden_stride", lambda N: 1)
+    assert _fails(tcb.test_fibsphere_codebook_pairs_radii_and_directions)

@@ -81,7 +81,8 @@ int fa_params(const fa_ctx *ctx, int *N, double *r, int *L);
 /* fa_vertex_table - copies the vertex table, double [N][2], to host memory V_host. Blocking. */
 int fa_vertex_table(const fa_ctx *ctx, double *V_host);
 
-/* fa_segments - anchors per stream of capacity T_cap: ceil(T_cap / L); -1 on bad arguments. */
+/* fa_segments - anchors per stream of capacity T_cap: ceil(T_cap / L); -1 on bad arguments (T_cap < 1 or
+ * within 64 of INT64_MAX). */
 int64_t fa_segments(const fa_ctx *ctx, int64_t T_cap);
 
 /*

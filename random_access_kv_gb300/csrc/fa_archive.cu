@@ -1,5 +1,5 @@
 // Iterated-map archive of symbol streams ("Fractal KV-Cache Archives", Method 1): encode / append,
-// full decode and random access, with the C ABI of include/fractal.h.
+// full decode and random access kernels and their launches (the C ABI is in fa_api.cu).
 //
 // Each segment of L symbols is independent (it starts at the origin), so one device thread owns one
 // segment (encode, decode) or one lookup (random access). The work is a chain of dependent fp64
@@ -14,38 +14,19 @@
 //     above fp32 error), the point is checked to lie within r + 3/4 of the margin of that cell's
 //     centre, then the map is inverted in fp64 as p = V + (p - V) / r with the quotient taken as a
 //     fused multiply by 1/r. The fp32 copy of the point is cut from the fp64 bits with integer
-//     instructions: a hardware fp64-to-fp32 conversion would take fp64 pipe cycles, which are
-//     the scarce resource here.
+//     instructions, which measured faster in these kernels than the hardware fp64-to-fp32
+//     conversion.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
-#include <stdlib.h>
 
-#include <vector>
-
-#include "fractal.h"
-
-struct fa_ctx {
-    int device = 0;
-    int N = 0;
-    int L = 0;
-    double r = 0.0;
-    double rinv = 0.0;
-    float scaleN = 0.f;     // N / (2 pi): angle to vertex index
-    float lim2 = 0.f;       // (r + 3/4 margin)^2: largest squared distance to a cell centre
-    int num_sms = 0;
-    double2 *V = nullptr;   // [N] vertices
-    float2 *Cf = nullptr;   // [N] cell centres (1 - r) V(c), fp32
-    uint32_t *flags = nullptr;
-};
+#include "fa_internal.h"
 
 namespace {
 
-constexpr int kThreads = 256;
+using fa::kMaxSegment;
+using fa::kThreads;
 constexpr uint16_t kBad = 0xFFFFu;
-constexpr int kMaxN = 4096;
-constexpr int kMaxSegment = 64;
-constexpr double kMinMargin = 2e-5;
 
 struct Tables {
     const double2 *V;
@@ -293,209 +274,38 @@ archive_access(Tables t, const double2 *__restrict__ anchors, int64_t n_streams,
     if (range) atomicOr(t.flags, (uint32_t)FA_FLAG_RANGE);
 }
 
-struct DeviceGuard {
-    int prev = -1;
-    bool changed = false;
-    cudaError_t err = cudaSuccess;
-    explicit DeviceGuard(int dev) {
-        err = cudaGetDevice(&prev);
-        if (err == cudaSuccess && prev != dev) {
-            err = cudaSetDevice(dev);
-            changed = err == cudaSuccess;
-        }
-    }
-    ~DeviceGuard() {
-        if (changed) cudaSetDevice(prev);
-    }
-};
-
-bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
-
-double cell_margin(int N, double r) { return (1.0 - r) * sin(M_PI / N) - r; }
-
-void free_ctx(fa_ctx *c) {
-    if (!c) return;
-    cudaFree(c->V);
-    cudaFree(c->Cf);
-    cudaFree(c->flags);
-    delete c;
-}
-
 unsigned blocks_for(int64_t threads) { return (unsigned)((threads + kThreads - 1) / kThreads); }
 
 }  // namespace
 
-extern "C" {
+namespace fa {
 
-double fa_ratio_limit(int N) {
-    if (N < 2) return 0.0;
-    const double s = sin(M_PI / N);
-    return s / (1.0 + s);
+cudaError_t launch_encode(const fa_ctx *c, const uint16_t *sym, int64_t n_streams, int64_t n_new, int64_t S_cap,
+                          int64_t T_old, int64_t s0, int64_t n_seg, double *anchors, cudaStream_t s) {
+    archive_encode<<<blocks_for(n_streams * n_seg), kThreads, 0, s>>>(tables_of(c), sym, n_streams, n_new, S_cap,
+                                                                     T_old, s0, n_seg,
+                                                                     reinterpret_cast<double2 *>(anchors));
+    return cudaGetLastError();
 }
 
-int fa_max_segment(int N, double r) {
-    if (N < 2 || !(r > 0.0) || !(r < fa_ratio_limit(N))) return 0;
-    const double u = ldexp(1.0, -53);
-    const double half_margin = 0.5 * cell_margin(N, r);
-    const double delta = 1.01 * u * (1.0 + 4.0 * r);     // forward step, per coordinate
-    const double eta = 8.0 * u;                           // backward step, per coordinate
-    // error bound of the rebuilt point after j backward steps: sqrt(2) (delta + r eta) r^-j / (1 - r)
-    double err = sqrt(2.0) * (delta + r * eta) / (1.0 - r);
-    if (!(err <= half_margin)) return 0;
-    int L = 1;                                            // decisions j = 0 .. L-1 all fit
-    while (L < kMaxSegment && err / r <= half_margin) {
-        err /= r;
-        ++L;
-    }
-    return L;
+cudaError_t launch_decode(const fa_ctx *c, const double *anchors, int64_t n_streams, int64_t S_cap, int64_t T,
+                          int64_t S, uint16_t *out, cudaStream_t s) {
+    archive_decode<<<blocks_for(n_streams * S), kThreads, 0, s>>>(
+        tables_of(c), reinterpret_cast<const double2 *>(anchors), n_streams, S_cap, T, S, out);
+    return cudaGetLastError();
 }
 
-int fa_create(fa_ctx **out, int N, double r, int L, int device) {
-    if (!out) return FQ_EINVAL;
-    *out = nullptr;
-    if (N < 2 || N > kMaxN || !isfinite(r) || !(r > 0.0) || !(r < fa_ratio_limit(N))) return FQ_EINVAL;
-    if (cell_margin(N, r) < kMinMargin || L < 1 || L > fa_max_segment(N, r)) return FQ_EINVAL;
-    int ndev = 0;
-    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) return FQ_ENODEV;
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return FQ_ENODEV;
-    if (prop.major != 10 || prop.minor != 3) return FQ_ENODEV;
-    DeviceGuard g(device);
-    if (g.err != cudaSuccess) return FQ_ECUDA;
-
-    fa_ctx *c = new fa_ctx();
-    c->device = device;
-    c->num_sms = prop.multiProcessorCount;
-    c->N = N;
-    c->L = L;
-    c->r = r;
-    c->rinv = 1.0 / r;
-    c->scaleN = (float)(N / (2.0 * M_PI));
-    const double lim = r + 0.75 * cell_margin(N, r);
-    c->lim2 = (float)(lim * lim);
-    std::vector<double2> V(N);
-    std::vector<float2> Cf(N);
-    for (int k = 0; k < N; ++k) {
-        const double a = 2.0 * M_PI * k / N;
-        V[k] = make_double2(cos(a), sin(a));
-        Cf[k] = make_float2((float)((1.0 - r) * V[k].x), (float)((1.0 - r) * V[k].y));
-    }
-    cudaError_t e = cudaMalloc((void **)&c->V, sizeof(double2) * N);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&c->Cf, sizeof(float2) * N);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
-    if (e != cudaSuccess) {
-        free_ctx(c);
-        return e == cudaErrorMemoryAllocation ? FQ_ENOMEM : FQ_ECUDA;
-    }
-    e = cudaMemcpy(c->V, V.data(), sizeof(double2) * N, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemcpy(c->Cf, Cf.data(), sizeof(float2) * N, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
-    if (e != cudaSuccess) {
-        free_ctx(c);
-        return FQ_ECUDA;
-    }
-    *out = c;
-    return FQ_OK;
-}
-
-int fa_params(const fa_ctx *ctx, int *N, double *r, int *L) {
-    if (!ctx) return FQ_EINVAL;
-    if (N) *N = ctx->N;
-    if (r) *r = ctx->r;
-    if (L) *L = ctx->L;
-    return FQ_OK;
-}
-
-int fa_vertex_table(const fa_ctx *ctx, double *V_host) {
-    if (!ctx || !V_host) return FQ_EINVAL;
-    DeviceGuard g(ctx->device);
-    if (g.err != cudaSuccess) return FQ_ECUDA;
-    return cudaMemcpy(V_host, ctx->V, sizeof(double2) * ctx->N, cudaMemcpyDeviceToHost) == cudaSuccess ? FQ_OK
-                                                                                                         : FQ_ECUDA;
-}
-
-int64_t fa_segments(const fa_ctx *ctx, int64_t T_cap) {
-    if (!ctx || T_cap < 1) return -1;
-    return (T_cap + ctx->L - 1) / ctx->L;
-}
-
-int fa_encode(fa_ctx *ctx, const uint16_t *sym, int64_t n_streams, int64_t n_new, int64_t T_cap, int64_t T_old,
-              double *anchors, void *stream) {
-    if (!ctx || n_streams < 0 || n_new < 0 || T_cap < 1 || T_old < 0 || T_old > T_cap - n_new) return FQ_EINVAL;
-    if (n_streams == 0 || n_new == 0) return FQ_OK;
-    if (!sym || !anchors) return FQ_EINVAL;
-    if (!aligned(sym, 2) || !aligned(anchors, 16)) return FQ_EALIGN;
-    const int64_t S_cap = fa_segments(ctx, T_cap);
-    const int64_t s0 = T_old / ctx->L, n_seg = (T_old + n_new - 1) / ctx->L - s0 + 1;
-    if (n_streams > INT64_MAX / S_cap || n_streams > INT64_MAX / n_new) return FQ_EINVAL;
-    const int64_t threads = n_streams * n_seg;
-    if ((threads + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
-    DeviceGuard g(ctx->device);
-    if (g.err != cudaSuccess) return FQ_ECUDA;
-    archive_encode<<<blocks_for(threads), kThreads, 0, (cudaStream_t)stream>>>(
-        tables_of(ctx), sym, n_streams, n_new, S_cap, T_old, s0, n_seg, reinterpret_cast<double2 *>(anchors));
-    return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
-}
-
-int fa_decode(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_cap, int64_t T, uint16_t *out,
-              void *stream) {
-    if (!ctx || n_streams < 0 || T_cap < 1 || T < 0 || T > T_cap) return FQ_EINVAL;
-    if (n_streams == 0 || T == 0) return FQ_OK;
-    if (!anchors || !out) return FQ_EINVAL;
-    if (!aligned(anchors, 16) || !aligned(out, 2)) return FQ_EALIGN;
-    const int64_t S_cap = fa_segments(ctx, T_cap), S = (T + ctx->L - 1) / ctx->L;
-    if (n_streams > INT64_MAX / S_cap || n_streams > INT64_MAX / T) return FQ_EINVAL;
-    const int64_t threads = n_streams * S;
-    if ((threads + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
-    DeviceGuard g(ctx->device);
-    if (g.err != cudaSuccess) return FQ_ECUDA;
-    archive_decode<<<blocks_for(threads), kThreads, 0, (cudaStream_t)stream>>>(
-        tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, S_cap, T, S, out);
-    return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
-}
-
-int fa_access(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_cap, int64_t T, const int64_t *pos,
-              int64_t n, uint16_t *out, void *stream) {
-    if (!ctx || n_streams < 0 || T_cap < 1 || T < 0 || T > T_cap || n < 0) return FQ_EINVAL;
-    if (n == 0) return FQ_OK;
-    if (!pos || !out || (!anchors && n_streams > 0 && T > 0)) return FQ_EINVAL;
-    if (!aligned(anchors, 16) || !aligned(pos, 8) || !aligned(out, 2)) return FQ_EALIGN;
-    const int64_t S_cap = fa_segments(ctx, T_cap);
-    if (n_streams > INT64_MAX / T_cap || n_streams > INT64_MAX / S_cap) return FQ_EINVAL;
-    if ((n + kThreads - 1) / kThreads > INT32_MAX) return FQ_EINVAL;
-    DeviceGuard g(ctx->device);
-    if (g.err != cudaSuccess) return FQ_ECUDA;
+cudaError_t launch_access(const fa_ctx *c, const double *anchors, int64_t n_streams, int64_t T_cap, int64_t S_cap,
+                          int64_t T, const int64_t *pos, int64_t n, uint16_t *out, cudaStream_t s) {
     // Queue length per warp: enough warps for about kAccessWarpsPerSm per SM, 4 to 16 lookups per lane.
-    int64_t per_lane = (n + 32LL * ctx->num_sms * kAccessWarpsPerSm - 1) / (32LL * ctx->num_sms * kAccessWarpsPerSm);
+    int64_t per_lane = (n + 32LL * c->num_sms * kAccessWarpsPerSm - 1) / (32LL * c->num_sms * kAccessWarpsPerSm);
     per_lane = per_lane < kAccessMinPerLane ? kAccessMinPerLane : (per_lane > kAccessMaxPerLane ? kAccessMaxPerLane : per_lane);
     const int per_warp = (int)(32 * per_lane);
     const int64_t warps = (n + per_warp - 1) / per_warp;
     const size_t smem = (size_t)(kThreads / 32) * per_warp * (sizeof(int64_t) + sizeof(uint16_t));
-    archive_access<<<blocks_for(warps * 32), kThreads, smem, (cudaStream_t)stream>>>(
-        tables_of(ctx), reinterpret_cast<const double2 *>(anchors), n_streams, T_cap, S_cap, T, pos, n, per_warp,
-        out);
-    return cudaGetLastError() == cudaSuccess ? FQ_OK : FQ_ECUDA;
+    archive_access<<<blocks_for(warps * 32), kThreads, smem, s>>>(tables_of(c), reinterpret_cast<const double2 *>(anchors),
+                                                                  n_streams, T_cap, S_cap, T, pos, n, per_warp, out);
+    return cudaGetLastError();
 }
 
-int fa_status(fa_ctx *ctx, void *stream, uint32_t *flags) {
-    if (!ctx || !flags) return FQ_EINVAL;
-    DeviceGuard g(ctx->device);
-    if (g.err != cudaSuccess) return FQ_ECUDA;
-    cudaStream_t s = (cudaStream_t)stream;
-    uint32_t h = 0;
-    cudaError_t e = cudaMemcpyAsync(&h, ctx->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flags, 0, sizeof(uint32_t), s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return FQ_ECUDA;
-    *flags = h;
-    return FQ_OK;
-}
-
-void fa_destroy(fa_ctx *ctx) {
-    if (!ctx) return;
-    DeviceGuard g(ctx->device);
-    cudaDeviceSynchronize();
-    free_ctx(ctx);
-}
-
-}  // extern "C"
+}  // namespace fa

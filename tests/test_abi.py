@@ -117,3 +117,17 @@ def test_codebook_load_accepts_k3_at_d96(L):
         assert rc == fb.FQ_EINVAL and not h
     rc, h = _load(L, np.zeros((64, 5)), np.eye(96))
     assert rc == fb.FQ_EINVAL
+
+
+def test_archive_segment_bound_agrees_with_the_oracle_everywhere(L):
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+    from oracle import fractal as ofa
+
+    @hyp.settings(max_examples=300, deadline=None, derandomize=True)
+    @hyp.given(st.integers(2, 4096), st.floats(0.0, 1.1))
+    def check(N, rho):
+        r = rho * ofa.ratio_limit(N)
+        assert L.fa_max_segment(N, r) == ofa.max_segment(N, r)
+
+    check()

@@ -176,3 +176,22 @@ def test_symbol_range_is_checked():
         fa.encode_segment([0, 4], 4, 0.1)
     with pytest.raises(IndexError):
         fa.access(np.zeros((1, 2, 2)), 5, 4, 0.1, 4, 0, 5)
+
+
+def test_round_trip_property_over_alphabets_ratios_and_strings():
+    """Any alphabet 2..4096, any ratio 10%..95% of the disjointness limit, any string of the
+    longest allowed segment: the backward search returns the string."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=150, deadline=None, derandomize=True)
+    @hyp.given(st.integers(2, 4096), st.floats(0.1, 0.95), st.integers(0, 2 ** 32 - 1))
+    def check(N, rho, seed):
+        r = rho * fa.ratio_limit(N)
+        L = fa.max_segment(N, r)
+        if L == 0:
+            return
+        sym = np.random.default_rng(seed).integers(0, N, size=L)
+        assert fa.decode_segment(fa.encode_segment(sym, N, r), L, N, r) == list(sym)
+
+    check()

@@ -2,7 +2,6 @@
 import numpy as np
 import pytest
 
-import synth
 from oracle import codebook as ocb
 from oracle import workloads as ow
 from random_access_kv_gb300 import codebook as pcb

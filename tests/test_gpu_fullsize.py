@@ -125,7 +125,6 @@ def test_attend_full_size_sampled_groups(cfg, qpg):
     """Fused attention at the workload's full size, in the benchmark's launch configuration (keys at
     rows [0, M), values at [M, 2M), one group per (layer, head)), over a random store; sampled
     groups checked against the oracle's fp64 attention over the decoded records."""
-    from oracle import attention  # noqa: F401  (the oracle module the check uses)
     w = synth.WORKLOADS[cfg]
     C, Pi = ow.codebook(cfg), ow.rotation(cfg)
     ctx = fq.fq_codebook_load(C, Pi)

@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <new>
 #include <vector>
 
 #include "fa_internal.h"
@@ -84,7 +85,8 @@ int fa_create(fa_ctx **out, int N, double r, int L, int device) {
     DeviceGuard g(device);
     if (g.err != cudaSuccess) return FQ_ECUDA;
 
-    fa_ctx *c = new fa_ctx();
+    fa_ctx *c = new (std::nothrow) fa_ctx();
+    if (!c) return FQ_ENOMEM;
     c->device = device;
     c->num_sms = prop.multiProcessorCount;
     c->N = N;
@@ -94,8 +96,16 @@ int fa_create(fa_ctx **out, int N, double r, int L, int device) {
     c->scaleN = (float)(N / (2.0 * M_PI));
     const double lim = r + 0.75 * cell_margin(N, r);
     c->lim2 = (float)(lim * lim);
-    std::vector<double2> V(N);
-    std::vector<float2> Cf(N);
+    // Host tables in std::vector: an allocation failure there must not cross the C ABI.
+    std::vector<double2> V;
+    std::vector<float2> Cf;
+    try {
+        V.resize(N);
+        Cf.resize(N);
+    } catch (...) {
+        free_ctx(c);
+        return FQ_ENOMEM;
+    }
     for (int k = 0; k < N; ++k) {
         const double a = 2.0 * M_PI * k / N;
         V[k] = make_double2(cos(a), sin(a));

@@ -4,6 +4,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <new>
 #include <vector>
 
 #include "fq_internal.h"
@@ -67,6 +68,48 @@ cudaError_t upload(T **dst, const std::vector<T> &src) {
 
 bool is_full(const fq_ctx *c) { return c->k == c->d; }
 
+// Derived tables of a context, built on the host in double precision and copied to the device;
+// the kernels' function attributes and launch plans.
+cudaError_t build_tables(fq_ctx *c, const float *C_host, const float *Pi_host) {
+    const int N = c->N, k = c->k, d = c->d;
+    std::vector<float> C(C_host, C_host + (size_t)N * k);
+    std::vector<float> P(Pi_host, Pi_host + (size_t)d * d);
+    std::vector<float> cc(N);
+    for (int n = 0; n < N; ++n) {
+        double s = 0;
+        for (int t = 0; t < k; ++t) s += (double)C[(size_t)n * k + t] * C[(size_t)n * k + t];
+        cc[n] = (float)s;
+    }
+    cudaError_t e = upload(&c->C, C);
+    if (e == cudaSuccess) e = upload(&c->cc, cc);
+    if (e == cudaSuccess) e = upload(&c->Pi, P);
+    if (e == cudaSuccess && is_full(c)) {
+        // Crot[n][i] = sum_j C[n][j] Pi[j][i]  (row n = Pi^T c_n), accumulated in double.
+        std::vector<float> R((size_t)N * d);
+        std::vector<double> acc(d);
+        for (int n = 0; n < N; ++n) {
+            for (int i = 0; i < d; ++i) acc[i] = 0.0;
+            for (int j = 0; j < d; ++j) {
+                const double cj = C[(size_t)n * d + j];
+                const float *prow = &P[(size_t)j * d];
+                for (int i = 0; i < d; ++i) acc[i] += cj * (double)prow[i];
+            }
+            for (int i = 0; i < d; ++i) R[(size_t)n * d + i] = (float)acc[i];
+        }
+        e = upload(&c->Crot, R);
+    }
+    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = is_full(c) ? fq::prepare_full(c) : fq::prepare_encode_blocks(c);
+    if (e == cudaSuccess && !is_full(c)) e = fq::prepare_decode_blocks(c);
+    if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
+    if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
+    if (e == cudaSuccess && is_full(c) && fq::full_tc_supported(c)) e = fq::prepare_full_tc(c);
+    if (e == cudaSuccess && !is_full(c) && !c->grid2 && fq::kq_tc_supported(c)) e = fq::prepare_kq_tc(c);
+    if (e == cudaSuccess) e = fq::prepare_attend(c);
+    return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -120,41 +163,15 @@ int fq_codebook_load(fq_ctx **out, const float *C_host, int N, int k, const floa
     c->num_sms = prop.multiProcessorCount;
     c->smem_optin = (int)prop.sharedMemPerBlockOptin;
 
-    std::vector<float> C(C_host, C_host + (size_t)N * k);
-    std::vector<float> P(Pi_host, Pi_host + (size_t)d * d);
-    std::vector<float> cc(N);
-    for (int n = 0; n < N; ++n) {
-        double s = 0;
-        for (int t = 0; t < k; ++t) s += (double)C[(size_t)n * k + t] * C[(size_t)n * k + t];
-        cc[n] = (float)s;
+    // Host tables are built in std::vector: an allocation failure there must not cross the C ABI.
+    cudaError_t e;
+    try {
+        e = build_tables(c, C_host, Pi_host);
+    } catch (const std::bad_alloc &) {
+        e = cudaErrorMemoryAllocation;
+    } catch (...) {
+        e = cudaErrorUnknown;
     }
-    cudaError_t e = upload(&c->C, C);
-    if (e == cudaSuccess) e = upload(&c->cc, cc);
-    if (e == cudaSuccess) e = upload(&c->Pi, P);
-    if (e == cudaSuccess && is_full(c)) {
-        // Crot[n][i] = sum_j C[n][j] Pi[j][i]  (row n = Pi^T c_n), accumulated in double.
-        std::vector<float> R((size_t)N * d);
-        std::vector<double> acc(d);
-        for (int n = 0; n < N; ++n) {
-            for (int i = 0; i < d; ++i) acc[i] = 0.0;
-            for (int j = 0; j < d; ++j) {
-                const double cj = C[(size_t)n * d + j];
-                const float *prow = &P[(size_t)j * d];
-                for (int i = 0; i < d; ++i) acc[i] += cj * (double)prow[i];
-            }
-            for (int i = 0; i < d; ++i) R[(size_t)n * d + i] = (float)acc[i];
-        }
-        e = upload(&c->Crot, R);
-    }
-    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
-    if (e == cudaSuccess) e = is_full(c) ? fq::prepare_full(c) : fq::prepare_encode_blocks(c);
-    if (e == cudaSuccess && !is_full(c)) e = fq::prepare_decode_blocks(c);
-    if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
-    if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
-    if (e == cudaSuccess && is_full(c) && fq::full_tc_supported(c)) e = fq::prepare_full_tc(c);
-    if (e == cudaSuccess && !is_full(c) && !c->grid2 && fq::kq_tc_supported(c)) e = fq::prepare_kq_tc(c);
-    if (e == cudaSuccess) e = fq::prepare_attend(c);
     if (e != cudaSuccess) {
         const int rc = (e == cudaErrorMemoryAllocation) ? FQ_ENOMEM : FQ_ECUDA;
         free_ctx(c);

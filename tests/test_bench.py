@@ -36,6 +36,26 @@ def test_committed_traffic_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.committed_traffic("encode_k2_tc", 2, 1) is None
 
 
+def test_committed_traffic_of_a_named_archive_workload(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (tmp_path / "random_access_kv_gb300").symlink_to(os.path.join(ROOT, "random_access_kv_gb300"))
+    h = bench.source_hash("archive_access")
+    (prof / "archive_access_kv-streams.md").write_text(
+        f"- source_hash: `{h}`\n- rows_per_launch: 1048576\n- dram_bytes_per_launch: 19202560\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.committed_traffic("archive_access", "kv-streams", 1 << 19) == pytest.approx(9601280.0)
+    assert bench.committed_traffic("archive_access", "document", 1 << 20) is None
+
+
+def test_archive_params_are_the_librarys_bound():
+    from oracle import fractal as ofa
+    from random_access_kv_gb300 import build as fbuild
+    fbuild.build()
+    r, L = bench.archive_params(256)
+    assert r == pytest.approx(0.75 * ofa.ratio_limit(256), rel=1e-15) and L == ofa.max_segment(256, r) == 7
+
+
 def test_reference_arm_prints_one_contract_line():
     p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "1",
                         "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)

@@ -73,3 +73,13 @@ def test_reference_arm_prints_on_rank_zero_only():
                         "--steps", "1", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
     assert p.returncode == 0, p.stderr[-2000:]
     assert p.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("mode", [["--archive"], ["--attend", "--workload", "2"], ["--rate-sweep"]])
+def test_other_modes_print_on_rank_zero_only(mode):
+    # The archive, attention and rate-sweep reference arms follow the same rule.
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", *mode,
+                        "--steps", "1", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    assert p.stdout.strip() == ""

@@ -195,3 +195,22 @@ def test_round_trip_property_over_alphabets_ratios_and_strings():
         assert fa.decode_segment(fa.encode_segment(sym, N, r), L, N, r) == list(sym)
 
     check()
+
+
+def test_cell_margin_is_the_distance_from_a_cell_to_its_sector_edges():
+    # Sample the boundary circle of cell c (radius r about (1 - r) V(c)) and measure each point's
+    # distance to the two rays that bound the sector of c (angles 2 pi c / N +- pi / N); the
+    # smallest distance is the margin g = (1 - r) sin(pi / N) - r.
+    for N, rho in ((3, 0.5), (16, 0.75), (256, 0.9)):
+        r = rho * fa.ratio_limit(N)
+        c = 5 % N
+        th = 2 * np.pi * c / N
+        centre = (1 - r) * np.array([np.cos(th), np.sin(th)])
+        phi = np.linspace(0, 2 * np.pi, 20001)
+        pts = centre[None] + r * np.stack([np.cos(phi), np.sin(phi)], axis=1)
+        dist = []
+        for edge in (th - np.pi / N, th + np.pi / N):
+            n = np.array([-np.sin(edge), np.cos(edge)])           # normal of the edge line
+            dist.append(np.abs(pts @ n))
+        got = np.min(np.minimum(*dist))
+        assert got == pytest.approx(fa.cell_margin(N, r), rel=1e-6, abs=1e-12)

@@ -20,7 +20,8 @@ metric is then cached K/V vectors read per second, and the line carries the atte
 cosine against the same attention over the uncompressed fp16 K/V.
 
 `--rate-sweep` measures relative MSE and encode/decode throughput against bits per coordinate,
-through the library, for the scalar Lloyd-Max codec (k = 1) and FibQuant at k = 2, 4, 8 and d.
+through the library, for the scalar Lloyd-Max codec (k = 1) and FibQuant at k = 2, 4, 8 and d;
+`--sweep-d 96` does it at d = 96 for k = 1, 2, 3 (the Fibonacci-sphere code) and 4.
 
 `--lloyd` times the workload's codebook construction: host numpy Lloyd against GPU Lloyd (the
 library's encoder assigns, `fq_centroid_sums` forms the centroids).
@@ -34,7 +35,8 @@ latency of one random access and of one appended symbol, each a single launch.
 `--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
 sample of the same workload instead.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2] [--attend]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+                    [--attend | --archive [--archive-workload W] | --rate-sweep [--sweep-d 96] | --lloyd]
 """
 from __future__ import annotations
 

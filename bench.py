@@ -1,17 +1,19 @@
 #!/usr/bin/env python3
 """Throughput of the FibQuant codec hot path on one GB300 (or N independent replicas).
 
-One step = the whole hot path over one batch of the GPT-2-small-shaped KV workload (the default;
-`--workload 1|3|4|5` times the other workloads the same way)
-(12 layers x 12 heads x 1024 tokens, d = 64, k = 2, N = 256, b = 4 bits per coordinate):
-encode all of K and all of V (2 x 147,456 vectors: norm, rotation, nearest codeword, fixed-
-address packing), then random-access decode of 65,536 uniformly drawn rows from each
-(gather, unpack, codeword lookup, inverse rotation, scaling). K and V share the codebook and
-live in one code store, so each step is one encode launch and one gather launch. Inputs are resident in HBM when
-the timed region starts; L2 is flushed (a 256 MB write) before every timed step, outside the
-step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it. A step's
-events bracket both launches (the decode is launched as a programmatic dependent of the encode);
-the roofline's per-kernel times come from each launch timed on its own, L2 flushed before it.
+One step = the whole hot path over one batch of the Llama-shaped long-context KV workload (the
+default; `--workload 1|2|3|5` times the other workloads the same way): 32 layers x 8 KV heads x
+32,768 tokens, d = 128, k = 8, N = 4096, b = 1.5 bits per coordinate. K and V arrive as a token
+stream: 32 appends, each encoding 1,024 new tokens of every (layer, head) sequence of both
+tensors (524,288 vectors per append: norm, rotation, nearest codeword, fixed-address packing),
+then a random-access decode of 3,277 token positions (10%) of every sequence (1,677,824 rows:
+gather, unpack, codeword lookup, inverse rotation, scaling). K and V share the codebook and live
+in one code store, so each append is one launch and the gather one launch. Inputs are resident in
+HBM when the timed region starts; L2 is flushed (a 256 MB write) before every timed step, outside
+the step's events. The metric is vectors/s (encoded + decoded), with fp16 GB/s beside it. A
+step's events bracket all of its launches; the roofline's per-kernel times come from each
+kernel's launches timed on their own, L2 flushed before them. `ms_per_step` is the mean of the K
+timed steps (their median is reported beside it).
 
 `--attend` times fused decode-into-attention instead: the workload's K and V are encoded into one
 store (untimed), then each step is one launch in which one fp16 query per (layer, head) group
@@ -35,7 +37,7 @@ latency of one random access and of one appended symbol, each a single launch.
 `--impl reference` times the CPU oracle (the plain fp64 statement of the codec) on a bounded
 sample of the same workload instead.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 2]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload 4]
                     [--attend | --archive [--archive-workload W] | --rate-sweep [--sweep-d 96] | --lloyd]
 """
 from __future__ import annotations
@@ -654,6 +656,8 @@ def run_ours(args) -> None:
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": conf,
+            "step_statistic": "mean over the timed steps (ms_per_step); median beside it",
+            "median_ms_per_step": statistics.median(step_ms),
             "fp16_gbps": value * 2 * d / 1e9,
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -1209,7 +1213,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--workload", type=int, default=4)
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--attend", action="store_true", help="time fused decode-into-attention")
     ap.add_argument("--rate-sweep", action="store_true",

@@ -176,18 +176,23 @@ int fq_centroid_sums(fq_ctx *ctx, const void *x, int64_t M, const float *nu, con
  */
 int fq_selftest_wait(fq_ctx *ctx, uint64_t limit_ns, void *stream);
 
-/* Number of uint32 words of a store of M records: ceil(M R / 32). Returns -1 on bad arguments. */
+/* Number of uint32 words of a store of M records: ceil(M R / 32), R = (d/k) log2 N bits per record
+ * at a fixed address per vector [FibQuant §1 fixed address; §2.3 rate]. Returns -1 on bad arguments. */
 int64_t fq_code_words(const fq_ctx *ctx, int64_t M);
 
 /* R = (d/k) log2 N, bits per record [FibQuant §2.3, rate]. Returns -1 for a NULL context. */
 int fq_record_bits(const fq_ctx *ctx);
 
-/* d, k and N of a context (any output pointer may be NULL). */
+/* d, k and N of a context (any output pointer may be NULL): head dimension, block size and codebook
+ * size of [FibQuant §2.3, encoder]. Returns FQ_EINVAL for a NULL context. */
 int fq_shape(const fq_ctx *ctx, int *d, int *k, int *N);
 
 /*
- * fq_status - synchronise `stream`, then read and clear the context's sticky device flags
- * (FQ_FLAG_*) into *flags. Returns FQ_ECUDA if the stream reports an error.
+ * fq_status - read and clear the context's sticky device flags (FQ_FLAG_*) into *flags, then
+ * synchronise `stream`. The read-and-clear is one atomic exchange on the device, ordered after the
+ * work already queued on `stream`; a flag raised at the same time by a kernel on another stream is
+ * either returned now or kept for the next call, never lost. Returns FQ_ECUDA if the stream reports
+ * an error. (Failure reporting of this library; the method's pages describe none.)
  */
 int fq_status(fq_ctx *ctx, void *stream, uint32_t *flags);
 

@@ -115,7 +115,8 @@ int fa_decode(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_c
 int fa_access(fa_ctx *ctx, const double *anchors, int64_t n_streams, int64_t T_cap, int64_t T,
               const int64_t *pos, int64_t n, uint16_t *out, void *stream);
 
-/* fa_status - reads and clears the context's sticky FA_FLAG_* bits (synchronises `stream`). */
+/* fa_status - reads and clears the context's sticky FA_FLAG_* bits in one atomic exchange on the device
+ * (as fq_status), then synchronises `stream`. */
 int fa_status(fa_ctx *ctx, void *stream, uint32_t *flags);
 
 /* fa_destroy - frees the context's device tables. NULL is a no-op. */

@@ -113,14 +113,14 @@ int fa_create(fa_ctx **out, int N, double r, int L, int device) {
     }
     cudaError_t e = cudaMalloc((void **)&c->V, sizeof(double2) * N);
     if (e == cudaSuccess) e = cudaMalloc((void **)&c->Cf, sizeof(float2) * N);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, 2 * sizeof(uint32_t));   // sticky word, taken copy
     if (e != cudaSuccess) {
         free_ctx(c);
         return e == cudaErrorMemoryAllocation ? FQ_ENOMEM : FQ_ECUDA;
     }
     e = cudaMemcpy(c->V, V.data(), sizeof(double2) * N, cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemcpy(c->Cf, Cf.data(), sizeof(float2) * N, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, 2 * sizeof(uint32_t));
     if (e != cudaSuccess) {
         free_ctx(c);
         return FQ_ECUDA;
@@ -212,8 +212,9 @@ int fa_status(fa_ctx *ctx, void *stream, uint32_t *flags) {
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t h = 0;
-    cudaError_t e = cudaMemcpyAsync(&h, ctx->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flags, 0, sizeof(uint32_t), s);
+    // One atomic read-and-clear on the device (see fq_status).
+    cudaError_t e = fq::launch_take_flags(ctx->flags, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, ctx->flags + 1, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return FQ_ECUDA;
     *flags = h;

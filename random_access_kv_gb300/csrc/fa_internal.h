@@ -18,8 +18,13 @@ struct fa_ctx {
     int num_sms = 0;
     double2 *V = nullptr;   // [N] vertices
     float2 *Cf = nullptr;   // [N] cell centres (1 - r) V(c), fp32
-    uint32_t *flags = nullptr;
+    uint32_t *flags = nullptr;   // [0] sticky FA_FLAG_* word, [1] the copy fa_status takes
 };
+
+namespace fq {
+// flags[1] = atomic exchange of flags[0] with 0, by one device thread (defined in fq_selftest.cu).
+cudaError_t launch_take_flags(uint32_t *flags, cudaStream_t s);
+}  // namespace fq
 
 namespace fa {
 

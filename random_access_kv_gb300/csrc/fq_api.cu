@@ -98,8 +98,9 @@ cudaError_t build_tables(fq_ctx *c, const float *C_host, const float *Pi_host) {
         }
         e = upload(&c->Crot, R);
     }
-    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, sizeof(uint32_t));
-    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, sizeof(uint32_t));
+    // flags[0]: the sticky word the kernels set; flags[1]: where fq_status takes it to.
+    if (e == cudaSuccess) e = cudaMalloc((void **)&c->flags, 2 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(c->flags, 0, 2 * sizeof(uint32_t));
     if (e == cudaSuccess) e = is_full(c) ? fq::prepare_full(c) : fq::prepare_encode_blocks(c);
     if (e == cudaSuccess && !is_full(c)) e = fq::prepare_decode_blocks(c);
     if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
@@ -326,8 +327,10 @@ int fq_status(fq_ctx *ctx, void *stream, uint32_t *flags) {
     if (g.err != cudaSuccess) return FQ_ECUDA;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t h = 0;
-    cudaError_t e = cudaMemcpyAsync(&h, ctx->flags, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ctx->flags, 0, sizeof(uint32_t), s);
+    // Read and clear in one atomic step on the device, so that a flag another stream's kernel
+    // raises meanwhile is kept for the next call rather than cleared unread.
+    cudaError_t e = fq::launch_take_flags(ctx->flags, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, ctx->flags + 1, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return FQ_ECUDA;
     *flags = h;

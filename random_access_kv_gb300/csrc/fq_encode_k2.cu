@@ -42,7 +42,6 @@ constexpr int kOvfMax = 12;
 constexpr int kCellBytes = (kGridR * kGridR * 4 + 15) & ~15;
 constexpr float kMagic = 12582912.f;       // 1.5 * 2^23: adding it rounds to an integer held in the low bits
 constexpr int kMagicBits = 0x4B400000;
-constexpr int kCluster = 4;                // CTAs that share one L2 read of the tables (multicast)
 
 template <int D, int NG, int NBUF>
 struct Layout {
@@ -189,32 +188,28 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // Shared tables: the cluster's CTAs each fetch a slice and multicast it to all of them, so the
-    // cluster reads them from L2 once. Pi has its own barrier so that the first rotation can start
-    // while the candidate grid is still arriving.
-    cluster_sync();                                   // every CTA's barriers are initialised
+    // Shared tables, each CTA its own copy by plain bulk copies. Pi has its own barrier so that
+    // the first rotation can start while the candidate grid is still arriving.
     if (tid == 0) {
         prefetch_tensormap(&xmap);
         const uint32_t cw_bytes = (uint32_t)p.N * 8u;
         const uint32_t tab_bytes = kCellBytes + kOvfSlots * 16u;
         mbar_arrive_expect_tx(bar_pi, 2u * L::kPiPart);
+        bulk_g2s(pi, p.pi_split, 2u * L::kPiPart, bar_pi);
         mbar_arrive_expect_tx(bar_grid, tab_bytes + cw_bytes);
-        const uint32_t r = cluster_ctarank();
-        const uint16_t all = (uint16_t)((1u << kCluster) - 1u);
-        auto slice = [&](void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-            const uint32_t per = ((bytes + kCluster - 1) / kCluster + 15u) & ~15u;
-            const uint32_t a = r * per, b = (a + per < bytes) ? a + per : bytes;
-            if (a < b)
-                bulk_g2s_multicast(static_cast<uint8_t *>(dst) + a, static_cast<const uint8_t *>(src) + a, b - a, bar,
-                                   all);
-        };
-        slice(pi, p.pi_split, 2u * L::kPiPart, bar_pi);
-        slice(grid, p.tables, tab_bytes, bar_grid);
-        slice(cw, p.cw, cw_bytes, bar_grid);
+        bulk_g2s(grid, p.tables, tab_bytes, bar_grid);
+        bulk_g2s(cw, p.cw, cw_bytes, bar_grid);
     }
     // Tables are in flight; x and the outputs may belong to the previous kernel in the stream.
     griddep_launch_dependents();
     griddep_wait();
+    // Loads and MMA commits issued and waited for, per barrier (every thread of a group keeps the
+    // same counts, the conditions being uniform over the group): after a timeout the cleanup
+    // waits on the parity of the phase still in flight.
+    uint32_t ld_issued[NBUF], ld_done[NBUF], mma_issued = 0, mma_done = 0;
+#pragma unroll
+    for (int i = 0; i < NBUF; ++i) ld_issued[i] = ld_done[i] = 0;
+    if (first < ntiles) ld_issued[0] = 1;
     // Each row group's first x tile.
     if (t == 0 && first < ntiles) {
         mbar_arrive_expect_tx(bar_load, (uint32_t)L::kXTile);
@@ -238,7 +233,9 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         uint8_t *xt = xbuf0 + buf * L::kXTile;
         ok = named_sync_and(1 + g, 128, mbar_wait(bar_load + buf, (uint32_t)((it / NBUF) & 1)));
         if (!ok) break;
+        ++ld_done[buf];
         const int64_t next = tile + gstride;
+        if (NBUF == 2 && next < ntiles) ++ld_issued[buf ^ 1];
         if (NBUF == 2 && t == 0 && next < ntiles) {
             // The other buffer's last readers (tile it-1: its MMA and the nu loads) finished
             // before the group barrier that closed iteration it-1.
@@ -264,6 +261,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
             }
             mma_commit(bar_mma);
         }
+        ++mma_issued;
         // nu of this thread's row, from the swizzled tile (chunk c of row t sits at chunk c ^ (t % 8)).
         float ss = 0.f;
 #pragma unroll
@@ -282,6 +280,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         }
         ok = named_sync_and(1 + g, 128, mbar_wait(bar_mma, (uint32_t)(it & 1)) && (it > 0 || mbar_wait(bar_grid, 0)));
         if (!ok) break;
+        ++mma_done;
         tc_fence_after();
 
         const int64_t r = tile * kTileRows + t;
@@ -355,6 +354,7 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
         }
         tc_fence_before();
         named_sync(1 + g, 128);
+        if (NBUF == 1 && next < ntiles) ++ld_issued[0];
         if (NBUF == 1 && t == 0 && next < ntiles) {
             mbar_arrive_expect_tx(bar_load, (uint32_t)L::kXTile);
 #pragma unroll
@@ -367,13 +367,16 @@ encode_k2_tc(const __grid_constant__ CUtensorMap xmap, const K2Params p) {
     if (it == 0) mbar_wait(bar_grid, 0);
     __syncthreads();
     if (!ok) {
-        // Give in-flight copies and MMAs a bounded chance to land before the CTA's memory goes away.
-        for (int i = 0; i < NBUF; ++i) mbar_wait(bar_load + i, 0, 1000000ull);
-        mbar_wait(bar_mma, 0, 1000000ull);
+        // Give in-flight copies and MMAs a bounded chance to land before the CTA's memory goes
+        // away: wait (briefly) on the phase each barrier still has outstanding.
+        mbar_wait(bar_pi, 0, 1000000ull);
+        mbar_wait(bar_grid, 0, 1000000ull);
+        for (int i = 0; i < NBUF; ++i)
+            if (ld_issued[i] > ld_done[i]) mbar_wait(bar_load + i, (ld_issued[i] - 1u) & 1u, 1000000ull);
+        if (mma_issued > mma_done) mbar_wait(bar_mma, (mma_issued - 1u) & 1u, 1000000ull);
     }
     tc_fence_after();
     if (tid < 32) tmem_dealloc(tmem_base, L::kTmemCols);
-    cluster_sync();                                   // no multicast from a peer is still landing
 }
 
 template <int D, int NG, int NBUF, int BS>
@@ -398,21 +401,16 @@ cudaError_t launch_k2(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     const int64_t ntiles = (M + kTileRows - 1) / kTileRows;
     int64_t grid = (ntiles + NG - 1) / NG;
     if (grid > ctx->k2_max_ctas) grid = ctx->k2_max_ctas;
-    grid = (grid + kCluster - 1) / kCluster * kCluster;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(NG * 128);
     cfg.dynamicSmemBytes = L::kBytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, encode_k2_tc<D, NG, NBUF, BS>, tm, p);
 }
 
@@ -423,23 +421,12 @@ cudaError_t prep_k2(fq_ctx *ctx) {
     cudaError_t e = cudaFuncSetAttribute(encode_k2_tc<D, NG, NBUF, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kBytes);
     if (e != cudaSuccess) return e;
-    // The persistent grid: as many clusters as can be resident at once.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(ctx->num_sms / kCluster * kCluster));
-    cfg.blockDim = dim3(NG * 128);
-    cfg.dynamicSmemBytes = L::kBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, encode_k2_tc<D, NG, NBUF, BS>, &cfg);
+    // The persistent grid: as many CTAs as can be resident at once (one per SM).
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_k2_tc<D, NG, NBUF, BS>, NG * 128, L::kBytes);
     if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
-    ctx->k2_max_ctas = clusters * kCluster;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    ctx->k2_max_ctas = per_sm * ctx->num_sms;
     return cudaSuccess;
 }
 
@@ -554,17 +541,17 @@ void split_operand_sw128(const float *src, int d, float scale, std::vector<uint1
 }
 
 bool encode_rows_tensor_map(CUtensorMap *tm, const void *x, int64_t M, int D) {
-    static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // The driver entry point, looked up once; a function-local static is initialised once even
+    // when contexts on several host threads encode at the same time.
+    static const PFN_cuTensorMapEncodeTiled_v12000 enc = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void *ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            enc = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-    }
+            return (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+        return nullptr;
+    }();
     if (!enc) return false;
     cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)M};
     cuuint64_t gstride[1] = {(cuuint64_t)D * 2};

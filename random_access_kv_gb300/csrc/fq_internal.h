@@ -17,13 +17,13 @@ struct fq_ctx {
     float *cc;                   // [N] |c_n|^2
     float *Pi;                   // [d x d] rotation, row-major
     float *Crot;                 // k == d: [N x d] rotated codebook C Pi (row n = Pi^T c_n)
-    uint32_t *flags;             // sticky FQ_FLAG_* word
+    uint32_t *flags;             // [0] sticky FQ_FLAG_* word, [1] the copy fq_status takes
     int num_sms;
     // k = 2 tensor-core encoder tables
     uint8_t *pi_split;           // fp16 halves of 2^12 Pi, swizzled as the MMA's B operand
     uint32_t *grid2;             // candidate grid and overflow slots
     float g_scale, g_offs;       // grid cell of u: round(u * g_scale + g_offs)
-    int k2_max_ctas;             // co-resident CTAs of the k = 2 encoder (whole clusters)
+    int k2_max_ctas;             // co-resident CTAs of the k = 2 encoder
     // tensor-core decoder tables
     uint8_t *pit_split;          // fp16 halves of 2^12 Pi^T, swizzled as the MMA's B operand
     uint16_t *cb_split;          // [N][2k] fp16 halves of 2^10 c_n (k hi, then k lo)
@@ -94,6 +94,9 @@ cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, R
 cudaError_t launch_centroid_sums(const fq_ctx *ctx, const __half *x, int64_t M, const float *nu,
                                  const uint32_t *codes, double *sums, double *counts, cudaStream_t s);
 cudaError_t launch_wait_selftest(const fq_ctx *ctx, uint64_t limit_ns, cudaStream_t s);
+// flags[1] = atomic exchange of flags[0] with 0, by one device thread: a read-and-clear of the
+// sticky word that loses no flag raised meanwhile by a kernel on another stream.
+cudaError_t launch_take_flags(uint32_t *flags, cudaStream_t s);
 cudaError_t prepare_attend(fq_ctx *ctx);
 cudaError_t launch_attend(const fq_ctx *ctx, const float *nu, const uint32_t *codes, const __half *q,
                           int64_t n_queries, int64_t q_per_group, int64_t T, int64_t k_row0, int64_t v_row0,

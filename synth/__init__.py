@@ -131,11 +131,17 @@ def kv_tensor(cfg: int, which: int = 0, rows: int | None = None) -> np.ndarray:
     if w.data == "gauss":
         n = w.rows if rows is None else min(rows, w.rows)
         return r.standard_normal((n, w.d), dtype=np.float32).astype(np.float16)
+    if w.data == "token_lognormal":
+        # Layers are drawn one after another, so a prefix needs only its first layers drawn.
+        per_layer = int(np.prod(w.shape[1:-1]))
+        n_layers = w.shape[0] if rows is None else min(w.shape[0], -(-rows // per_layer))
+        shape = (n_layers,) + tuple(w.shape[1:])
+        out = np.empty((n_layers * per_layer, w.d), dtype=np.float16)
+        _token_lognormal(r, shape, out)
+        return out if rows is None or rows >= out.shape[0] else out[:rows].copy()
     out = np.empty((w.rows, w.d), dtype=np.float16)
     if w.data == "channel_scaled":
         _channel_scaled(r, w.shape, out)
-    elif w.data == "token_lognormal":
-        _token_lognormal(r, w.shape, out)
     else:
         raise ValueError(w.data)
     return out if rows is None else out[:rows].copy()

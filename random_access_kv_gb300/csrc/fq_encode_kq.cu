@@ -1,26 +1,32 @@
 // Tensor-core block encoder for k = 4 and k = 8 [FibQuant §2.3, encoder].
 //
-// Per CTA: 16 consumer warps over one 128-row tile (warp w owns TMEM lanes 32 (w % 4)..+31, i.e.
-// its rows, and column quarter w / 4 of every score item) and a producer warp.
-// For every 128-row tile of x:
-//   1. Rotation as in the k = 2 encoder: TMA x tile (128-byte swizzle), tcgen05.mma of x against
-//      fp16 hi/lo halves of 2^12 Pi into TMEM; nu from the shared-memory tile.
-//   2. Each thread turns its row of u = Y / (2^12 nu) into one A-operand row per block b:
+// Persistent CTAs, one per SM: 8 consumer warps (two per TMEM lane quarter), a loader warp (bulk
+// and TMA copies) and an MMA warp. For every 128-row tile of x, in passes of NBH blocks:
+//   1. Rotation item: tcgen05.mma of the x tile (TMA, 128-byte swizzle) against fp16 hi/lo halves
+//      of 2^12 Pi into a TMEM buffer. Products of fp16 values are exact and the sums fp32, so Y
+//      carries fp32 accuracy. The consumers take nu from the shared-memory tile (first pass), read
+//      this pass's columns of Y and write one A-operand row per block b and row t:
 //          A_b = [uh, ul, uh, 2^10, 2^10, 0...],   uh + ul = fp16 hi/lo halves of 2^10 u_b,
 //      while every codeword n is a B-operand row
 //          B_n = [ch, ch, cl, hh, hl, 0...],        ch + cl = halves of 2^10 (-2 c_n),
 //                                                  hh + hl = halves of 2^10 |c_n|^2,
-//      so one MMA of K = 16 (k = 4) or K = 32 (k = 8) gives 2^20 (|c_n|^2 - 2 u_b.c_n) for 128 rows
-//      and 128 codewords, with fp32 accumulation of exact fp16 products (the dropped ul*cl term
-//      is below 2^-22 of the result). |u_b - c_n|^2 differs from it by |u_b|^2, common to all n.
-//   3. The codebook streams through a shared-memory ring in 128-codeword tiles (producer warp,
-//      bulk copies); two TMEM score buffers let the MMA of one (tile, block) item overlap the
-//      argmin of the previous one. Each warp keeps a running minimum per (block, row) over its
-//      column quarter: per 16-column chunk a min-tree, and only when the quarter improves on its
-//      best so far, a search for its lowest index. The four quarters merge at the end of a pass
-//      (lowest score, then lowest index: ties go to the lowest n).
-//   4. Indices are packed at the record's fixed bit address; nu is stored.
-// Blocks are handled in passes of NBH so that their A operands fit in shared memory.
+//      so one MMA of K = 16 (k = 4) or K = 32 (k = 8) gives 2^20 (|c_n|^2 - 2 u_b.c_n) for 128
+//      rows and 128 codewords (the dropped ul*cl term is below 2^-22 of the result). This orders
+//      the codewords as |u_b - c_n|^2 does: the two differ by |u_b|^2, common to all n.
+//   2. Score items: for each 128-codeword tile of the codebook (resident in shared memory when
+//      it fits, else streamed through a ring) and each block of the pass, one MMA into one of
+//      four 128-column TMEM buffers. Consumer warp q (0 or 1) of a lane quarter takes the items
+//      of the blocks b = q mod 2: it reads its 32 rows x 128 scores, releases the buffer and
+//      folds the scores into a running (smallest score, 16-codeword chunk holding it) per (row,
+//      block): per chunk an 8-instruction tree of 3-input minima, one compare and two selects.
+//      Ties keep the earlier chunk.
+//   3. Resolution: at the end of the pass each (row, block) knows the chunk that holds its
+//      smallest tensor-core score. The 16 codewords of that chunk are scored again on the CUDA
+//      cores by squared difference |u_b - c_n|^2 in fp32 (u_b = (uh + ul) / 2^10, the values the
+//      MMA used), lowest score first, ties to the lowest n. The codeword found is within twice
+//      the tensor-core scores' rounding (about 2^-22 of |c|^2 + 2|u.c|) of the true nearest one.
+//   4. Indices are staged in shared memory and packed at the record's fixed bit address; nu is
+//      stored.
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <string.h>
@@ -38,19 +44,22 @@ namespace {
 using namespace sm100;
 
 constexpr int kRows = 128;
-constexpr int kStages = 4;
-constexpr int kCQ = 4;                    // consumer warps per lane quarter (column quarters of an item)
-constexpr int kSB = 3;                    // TMEM score buffers (MMAs in flight ahead of the readers)
-constexpr int kConsumerWarps = 4 * kCQ;
+constexpr int kNT = 128;                  // codewords per B tile (the MMA's N)
+constexpr int kChunk = 16;                // codewords per tracked chunk
+constexpr int kChunks = kNT / kChunk;     // chunks per item
+constexpr int kBufs = 4;                  // TMEM score buffers of kNT columns
+constexpr int kConsumerWarps = 8;
 constexpr int kThreads = kConsumerWarps * 32 + 64;      // + the loader warp and the MMA warp
+constexpr uint32_t kCons = kConsumerWarps * 32;
 constexpr float kPiScale = 4096.f;        // 2^12 on Pi
 constexpr float kOpScale = 1024.f;        // 2^10 on u, -2c and |c|^2
+constexpr int kSmemBudget = 227 * 1024;
 
-template <int D, int K, int NBH, int NT>
+template <int D, int K, int NBH>
 struct KQ {
-    static constexpr int kNT = NT;                                // codewords per B tile (MMA N)
     static constexpr int NB = D / K;
     static constexpr int NPASS = NB / NBH;
+    static constexpr int kPassCols = NBH * K;                     // Y columns one pass reads
     static constexpr int KP = (3 * K + 2 <= 16) ? 16 : 32;        // padded K of one block's operand
     static constexpr int kPiPart = D * D * 2;
     static constexpr int kXTile = kRows * D * 2;
@@ -59,19 +68,21 @@ struct KQ {
     static constexpr int oPi = 0;
     static constexpr int oX = oPi + 2 * kPiPart;
     static constexpr int oA = oX + kXTile;
-    static constexpr int oB = oA + NBH * kABlock;
-    static constexpr int oState = oB + kStages * kBTile;         // per (block, quarter, row): best, index
-    static constexpr int oBar = oState + NBH * kCQ * kRows * 8;
-    // bars: pi, x, rot, a_ready, rot_free, ready[kSB], free[kSB], full[kStages], empty[kStages]
-    static constexpr int kBars = 5 + 2 * kSB + 2 * kStages;
+    static constexpr int oIdx = oA + NBH * kABlock;               // uint16 [kRows][NB]
+    static constexpr int oRing = oIdx + ((kRows * NB * 2 + 1023) & ~1023);
+    static constexpr int kTail = 512 + 16 + 1024;                 // barriers, TMEM slot, alignment slack
+    static constexpr int kStagesFit = (kSmemBudget - oRing - kTail) / kBTile;
+    static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
+    static constexpr int oBar = oRing + kStages * kBTile;
+    // bars: pi, x, a_ready, drain, ready[kBufs], freeb[kBufs], full[kStages], empty[kStages]
+    static constexpr int kBars = 4 + 2 * kBufs + 2 * kStages;
     static constexpr int oTmem = oBar + kBars * 8;
     static constexpr int kBytes = oTmem + 16 + 1024;
-    // TMEM: kSB score buffers of kNT columns, then the rotation (so that the next tile's rotation
-    // can run while the last scores are read).
-    static constexpr int kRotCol = kSB * kNT;
-    static constexpr int kCols = kRotCol + D;
-    static constexpr uint32_t kTmemCols = kCols <= 256 ? 256 : 512;
-    static_assert(kCols <= 512, "tensor memory");
+    static_assert(kStages >= 2, "codebook ring");
+    static_assert(kBars * 8 <= 512, "barrier space");
+    static_assert(kPassCols == 64, "one pass reads 64 columns of Y");
+    static_assert(D <= kNT, "the rotation fits one score buffer");
+    static_assert(NBH % 2 == 0, "two consumer warps alternate over the blocks");
 };
 
 struct KQParams {
@@ -80,6 +91,7 @@ struct KQParams {
     int N, B;
     const uint8_t *pi_split;   // fp16 halves of 2^12 Pi, swizzled (as the k = 2 encoder)
     const uint8_t *cb_ops;     // [N / kNT] tiles of B rows, no-swizzle K-major core-matrix layout
+    const float *C;            // [N x K] fp32 codebook (chunk resolution)
     float *nu;
     uint32_t *codes;
     uint32_t *flags;
@@ -96,61 +108,70 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_noswz(uint32_t saddr, uint32_t 
     return d;                                          // layout type 0: no swizzle
 }
 
-template <int D, int K, int NBH, int NT>
+__device__ __forceinline__ float h2f_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float h2f_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+template <int D, int K, int NBH>
 __global__ void __launch_bounds__(kThreads, 1)
 encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
-    using L = KQ<D, K, NBH, NT>;
-    constexpr int kNT = NT;
-    constexpr int KP = L::KP;
-    constexpr int kQC = kNT / kCQ;             // columns of an item read by one warp
+    using L = KQ<D, K, NBH>;
+    constexpr int KP = L::KP, NB = L::NB, NPASS = L::NPASS, S = L::kStages;
+    constexpr int OWN = NBH / 2;                       // blocks of a pass one consumer warp owns
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
-    uint64_t *bar_pi = bars + 0, *bar_x = bars + 1, *bar_rot = bars + 2;
-    uint64_t *a_ready = bars + 3, *rot_free = bars + 4;
-    uint64_t *ready = bars + 5, *freeb = bars + 5 + kSB;              // [kSB] each
-    uint64_t *full = bars + 5 + 2 * kSB, *empty = bars + 5 + 2 * kSB + kStages;
+    uint64_t *bar_pi = bars + 0, *bar_x = bars + 1, *a_ready = bars + 2, *drain = bars + 3;
+    uint64_t *ready = bars + 4, *freeb = bars + 4 + kBufs;
+    uint64_t *full = bars + 4 + 2 * kBufs, *empty = bars + 4 + 2 * kBufs + S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
     uint8_t *xt = sm + L::oX;
-    float *st_best = reinterpret_cast<float *>(sm + L::oState);
-    uint32_t *st_bi = reinterpret_cast<uint32_t *>(sm + L::oState + NBH * kCQ * kRows * 4);
+    uint8_t *ring = sm + L::oRing;
+    uint16_t *idx_s = reinterpret_cast<uint16_t *>(sm + L::oIdx);
 
     const int tid = threadIdx.x;
     const int warp = tid / 32;
     const int lane = tid & 31;
     const int64_t ntiles = (p.M + kRows - 1) / kRows;
     const int nbt = p.N / kNT;
-    constexpr uint32_t kCons = kConsumerWarps * 32;
+    const bool resident = nbt <= S;                   // the whole codebook fits the ring
 
     if (tid == 0) {
         mbar_init(bar_pi, 1);
         mbar_init(bar_x, 1);
-        mbar_init(bar_rot, 1);
-        mbar_init(a_ready, kConsumerWarps);
-        mbar_init(rot_free, kConsumerWarps);
-        for (int b = 0; b < kSB; ++b) {
+        mbar_init(a_ready, 1);
+        mbar_init(drain, 1);
+        for (int b = 0; b < kBufs; ++b) {
             mbar_init(ready + b, 1);
-            mbar_init(freeb + b, kConsumerWarps);
+            mbar_init(freeb + b, 4);                  // one warp per lane quarter reads an item
         }
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, 1);
         }
         fence_barrier_init();
     }
-    if (warp == 0) tmem_alloc(tmem_slot, L::kTmemCols);
+    if (warp == 0) tmem_alloc(tmem_slot, 512);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t rot_acc = tmem_base + (uint32_t)L::kRotCol;
+    // The next kernel in the stream may start its prologue; it waits for this grid before it
+    // touches memory this one writes.
+    griddep_launch_dependents();
 
     if (warp == kConsumerWarps) {
-        // Loader: Pi, the first x tile, then the codebook tiles in the order they are used.
+        // Loader: Pi and (when resident) the whole codebook, then the first x tile, then the
+        // codebook tiles in the order the MMA warp uses them.
         if (lane == 0) {
             prefetch_tensormap(&xmap);
             mbar_arrive_expect_tx(bar_pi, 2u * L::kPiPart);
             bulk_g2s(sm + L::oPi, p.pi_split, 2u * L::kPiPart, bar_pi);
+            if (resident)
+                for (int bt = 0; bt < nbt; ++bt) {
+                    mbar_arrive_expect_tx(full + bt, (uint32_t)L::kBTile);
+                    bulk_g2s(ring + bt * L::kBTile, p.cb_ops + (size_t)bt * L::kBTile, L::kBTile, full + bt);
+                }
+            griddep_wait();                           // x may be written by the previous kernel
             if ((int64_t)blockIdx.x < ntiles) {
                 mbar_arrive_expect_tx(bar_x, (uint32_t)L::kXTile);
 #pragma unroll
@@ -159,54 +180,67 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
             }
             uint32_t k = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x)
-                for (int pass = 0; pass < L::NPASS && ok; ++pass)
-                    for (int bt = 0; bt < nbt && ok; ++bt, ++k) {
-                        const uint32_t s = k % kStages, round = k / kStages;
-                        if (round > 0) ok = mbar_wait(empty + s, (round - 1) & 1);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(full + s, (uint32_t)L::kBTile);
-                        bulk_g2s(sm + L::oB + s * L::kBTile, p.cb_ops + (size_t)bt * L::kBTile, L::kBTile, full + s);
-                    }
+            if (!resident)
+                for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x)
+                    for (int pass = 0; pass < NPASS && ok; ++pass)
+                        for (int bt = 0; bt < nbt; ++bt, ++k) {
+                            const uint32_t s = k % S, round = k / S;
+                            if (round > 0) ok = mbar_wait(empty + s, (round - 1) & 1);
+                            if (!ok) break;
+                            mbar_arrive_expect_tx(full + s, (uint32_t)L::kBTile);
+                            bulk_g2s(ring + s * L::kBTile, p.cb_ops + (size_t)bt * L::kBTile, L::kBTile, full + s);
+                        }
             if (!ok) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+            // Every copy issued into the ring has landed before the CTA can exit (at once on the
+            // normal path, where the MMA warp consumed them all).
+            const uint32_t issued = resident ? (uint32_t)nbt : k;
+            for (uint32_t s = 0; s < (uint32_t)S && s < issued; ++s) {
+                const uint32_t n_s = (issued - 1 - s) / S + 1;              // copies into stage s
+                mbar_wait(full + s, (n_s - 1) & 1, ok ? 2000000000ull : 1000000ull);
+            }
         }
     } else if (warp == kConsumerWarps + 1) {
-        // MMA issuer: the rotation of each tile, then its score items in order.
+        // MMA issuer: per pass a rotation item, then the score items in (tile, block) order.
         if (lane == 0) {
             const uint32_t idesc_rot = idesc_f16_f32(128, D);
             const uint32_t idesc_sc = idesc_f16_f32(128, kNT);
             const uint32_t pi_hi = smem_addr(sm + L::oPi), pi_lo = pi_hi + L::kPiPart;
-            const uint32_t a_base = smem_addr(sm + L::oA), b_base = smem_addr(sm + L::oB);
+            const uint32_t a_base = smem_addr(sm + L::oA), b_base = smem_addr(ring);
             bool ok = mbar_wait(bar_pi, 0);
-            uint32_t k = 0, item = 0, npass = 0;
+            uint32_t gi = 0, k = 0, npass = 0;
             int64_t it = 0;
             for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-                ok = mbar_wait(bar_x, (uint32_t)(it & 1));
-                // The consumers have read the previous tile's rotation.
-                if (ok && it > 0) ok = mbar_wait(rot_free, (uint32_t)((it - 1) & 1));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t xa = smem_addr(xt);
+                for (int pass = 0; pass < NPASS && ok; ++pass, ++npass) {
+                    uint32_t buf = gi % kBufs;
+                    if (gi >= kBufs) ok = mbar_wait(freeb + buf, (gi / kBufs - 1) & 1);
+                    if (ok && pass == 0) ok = mbar_wait(bar_x, (uint32_t)(it & 1));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t xa = smem_addr(xt);
+                    const uint32_t rot = tmem_base + buf * (uint32_t)kNT;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t pb = half ? pi_lo : pi_hi;
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t pb = half ? pi_lo : pi_hi;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                        const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
-                        mma_f16(rot_acc, sdesc_sw128(xa + koff), sdesc_sw128(pb + boff), idesc_rot, (half | kk) ? 1u : 0u);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t koff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
+                            const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
+                            mma_f16(rot, sdesc_sw128(xa + koff), sdesc_sw128(pb + boff), idesc_rot,
+                                    (half | kk) ? 1u : 0u);
+                        }
                     }
-                }
-                mma_commit(bar_rot);
-                for (int pass = 0; pass < L::NPASS && ok; ++pass, ++npass) {
+                    mma_commit(ready + buf);
+                    ++gi;
+                    // The consumers have written this pass's A operands (and read the rotation).
                     ok = mbar_wait(a_ready, npass & 1);
-                    for (int bt = 0; bt < nbt && ok; ++bt, ++k) {
-                        const uint32_t s = k % kStages;
-                        ok = mbar_wait(full + s, (k / kStages) & 1);
-                        for (int bb = 0; bb < NBH && ok; ++bb, ++item) {
-                            const uint32_t buf = item % kSB;
-                            // Buffer `buf` was last filled by item - kSB; wait until it has been read.
-                            if (item >= kSB) ok = mbar_wait(freeb + buf, ((item - kSB) / kSB) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int bt = 0; bt < nbt && ok; ++bt) {
+                        const uint32_t s = resident ? (uint32_t)bt : k % S;
+                        ok = mbar_wait(full + s, resident ? 0u : (k / S) & 1);
+                        for (int bb = 0; bb < NBH && ok; ++bb) {
+                            buf = gi % kBufs;
+                            if (gi >= kBufs) ok = mbar_wait(freeb + buf, (gi / kBufs - 1) & 1);
                             if (!ok) break;
                             tc_fence_after();
                             const uint32_t aa = a_base + (uint32_t)(bb * L::kABlock);
@@ -217,200 +251,249 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                                 mma_f16(dst, sdesc_kmajor_noswz(aa + kk * 256, (KP / 8) * 128),
                                         sdesc_kmajor_noswz(ba + kk * 256, (KP / 8) * 128), idesc_sc, kk ? 1u : 0u);
                             mma_commit(ready + buf);
+                            ++gi;
                         }
-                        if (ok) mma_commit(empty + s);
+                        if (!resident) {
+                            if (ok) mma_commit(empty + s);
+                            ++k;
+                        }
                     }
                 }
             }
             if (!ok) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+            // Every MMA issued has completed before the CTA can exit.
+            mma_commit(drain);
+            mbar_wait(drain, 0, ok ? 2000000000ull : 1000000ull);
         }
     } else {
-        // Consumers: warp w reads TMEM lanes 32 (w % 4) .. +31 (its rows) and column quarter w / 4
-        // of every score item.
+        // Consumers: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. rows t of the tile, and owns
+        // the blocks b = w / 4 (mod 2) of every pass.
         const int lq = warp % 4, cq = warp / 4;
-        const int t = 32 * lq + lane;             // row within the tile = TMEM lane
-        const bool lead = tid == 0;
+        const int t = 32 * lq + lane;
         const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
-        const int R = L::NB * p.B;
-        uint32_t item = 0;
+        const int R = NB * p.B;
+        griddep_wait();                               // the code store may be the previous kernel's
+        uint32_t gi = 0;
         bool ok = true;
         int64_t it = 0;
+        uint32_t x_issued = (int64_t)blockIdx.x < ntiles ? 1u : 0u, x_done = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
-            ok = mbar_wait(bar_x, (uint32_t)(it & 1));
-            float ss = 0.f;
-            if (ok) {
-#pragma unroll
-                for (int kb = 0; kb < D / 64; ++kb) {
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(xt + kb * 16384 + t * 128 + ((c ^ (t & 7)) << 4));
-                        const __half2 *h2 = reinterpret_cast<const __half2 *>(&v);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float2 f = __half22float2(h2[q]);
-                            ss = fmaf(f.x, f.x, ss);
-                            ss = fmaf(f.y, f.y, ss);
-                        }
-                    }
-                }
-            }
-            ok = named_sync_and(1, kCons, ok && mbar_wait(bar_rot, (uint32_t)(it & 1)));
-            if (!ok) break;
-            tc_fence_after();
-            // nu is read and the rotation has consumed the x tile: fetch the next one.
-            const int64_t next = tile + gridDim.x;
-            if (lead && next < ntiles) {
-                mbar_arrive_expect_tx(bar_x, (uint32_t)L::kXTile);
-#pragma unroll
-                for (int kb = 0; kb < D / 64; ++kb)
-                    tma_load_2d(xt + kb * 16384, &xmap, kb * 64, (int)(next * kRows), bar_x);
-            }
-            const bool finite = isfinite(ss);
-            const float nu = finite ? sqrtf(ss) : 0.f;
-            const float us = nu > 0.f ? (kOpScale / kPiScale) / nu : 0.f;     // 2^10 u = Y * us
             const int64_t r = tile * kRows + t;
             const bool live = r < p.M;
-            const int64_t orow = live ? p.map(r) : 0;
-            BitWriter wr(p.codes, orow * (int64_t)R);
-
-            for (int pass = 0; pass < L::NPASS && ok; ++pass) {
-                // A operands of this pass's blocks (this warp: blocks cq, cq + 4, ...), row t of each.
-#pragma unroll
-                for (int j = 0; j < NBH / kCQ; ++j) {
-                    const int bb = j * kCQ + cq;
-                    const int b = pass * NBH + bb;
-                    float v[K];
-                    float w16[16];
-                    tmem_ld16(rot_acc + lane_off + (uint32_t)((b * K / 16) * 16), w16);
-                    tmem_wait_ld();
-                    const int off = (b * K) % 16;                    // run-time: pick with static indices
-#pragma unroll
-                    for (int o = 0; o < 16; o += K)
-                        if (off == o) {
-#pragma unroll
-                            for (int q = 0; q < K; ++q) v[q] = w16[o + q] * us;
-                        }
-                    uint32_t uh[K / 2], ul[K / 2];
-#pragma unroll
-                    for (int q = 0; q < K / 2; ++q) split_half2(v[2 * q], v[2 * q + 1], uh[q], ul[q]);
-                    const uint32_t one2 = 0x64006400u;                // (1024, 1024) in fp16
-                    uint8_t *arow = sm + L::oA + bb * L::kABlock + (t / 8) * (KP / 8) * 128 + (t % 8) * 16;
-                    if constexpr (K == 4) {
-                        *reinterpret_cast<uint4 *>(arow) = make_uint4(uh[0], uh[1], ul[0], ul[1]);
-                        *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(uh[0], uh[1], one2, 0u);
-                    } else {
-                        *reinterpret_cast<uint4 *>(arow) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-                        *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
-                        *reinterpret_cast<uint4 *>(arow + 256) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-                        *reinterpret_cast<uint4 *>(arow + 384) = make_uint4(one2, 0u, 0u, 0u);
-                    }
-                }
-                for (int bb = 0; bb < NBH; ++bb) {
-                    st_best[(bb * kCQ + cq) * kRows + t] = INFINITY;
-                    st_bi[(bb * kCQ + cq) * kRows + t] = 0u;
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(a_ready);
-                    if (pass == L::NPASS - 1) mbar_arrive(rot_free);
-                }
-
-                const int items = nbt * NBH;
-#pragma unroll 1
-                for (int i = 0; i < items; ++i, ++item) {
-                    const uint32_t buf = item % kSB;
-                    const int bt = i / NBH, bb = i % NBH;
-                    bool w = mbar_wait(ready + buf, (item / kSB) & 1);
-                    w = __all_sync(0xffffffffu, w);
-                    if (!w) {
-                        ok = false;
-                        break;
-                    }
+            float nu = 0.f, us = 0.f;
+            bool finite = true;
+            for (int pass = 0; pass < NPASS && ok; ++pass) {
+                // --- rotation item: nu (first pass), then this pass's A operands ---------------
+                {
+                    const uint32_t buf = gi % kBufs;
+                    bool w = mbar_wait(ready + buf, (gi / kBufs) & 1);
+                    if (pass == 0) w = w && mbar_wait(bar_x, (uint32_t)(it & 1));
+                    ok = named_sync_and(1, kCons, w);
+                    if (!ok) break;
+                    if (pass == 0) ++x_done;
                     tc_fence_after();
-                    float *pb = st_best + (bb * kCQ + cq) * kRows + t;
-                    uint32_t *pi = st_bi + (bb * kCQ + cq) * kRows + t;
-                    float best = *pb;
-                    // This warp's kQC columns of the item, all loads in flight before one wait.
-                    uint32_t rr[kQC / 32][32];
+                    if (pass == 0) {
+                        float ss = 0.f;
 #pragma unroll
-                    for (int h = 0; h < kQC / 32; ++h)
-                        tmem_ld32_nowait(tmem_base + lane_off + (uint32_t)(buf * kNT + cq * kQC + 32 * h), rr[h]);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(freeb + buf);      // the buffer's scores are in registers
-                    float cm[kQC / 16];
+                        for (int kb = 0; kb < D / 64; ++kb) {
 #pragma unroll
-                    for (int c = 0; c < kQC / 16; ++c) {
-                        float v16[16];
+                            for (int c = 0; c < 8; ++c) {
+                                const uint4 v =
+                                    *reinterpret_cast<const uint4 *>(xt + kb * 16384 + t * 128 + ((c ^ (t & 7)) << 4));
+                                const __half2 *h2 = reinterpret_cast<const __half2 *>(&v);
 #pragma unroll
-                        for (int z = 0; z < 16; ++z) v16[z] = __uint_as_float(rr[c / 2][16 * (c % 2) + z]);
-                        cm[c] = min16(v16);
-                    }
-                    float qmin = cm[0];
-#pragma unroll
-                    for (int c = 1; c < kQC / 16; ++c) qmin = fminf(qmin, cm[c]);
-                    if (qmin < best) {
-                        // The lowest column of this quarter holding the minimum: first the
-                        // 16-column chunk (from the chunk minima), then the column within it.
-                        int c0 = kQC / 16 - 1;
-#pragma unroll
-                        for (int c = kQC / 16 - 1; c >= 0; --c)
-                            if (cm[c] == qmin) c0 = c;
-                        uint32_t j = 15;
-#pragma unroll
-                        for (int c = 0; c < kQC / 16; ++c)
-                            if (c == c0) {
-#pragma unroll
-                                for (int z = 15; z >= 0; --z)
-                                    if (__uint_as_float(rr[c / 2][16 * (c % 2) + z]) == qmin) j = (uint32_t)z;
+                                for (int q = 0; q < 4; ++q) {
+                                    const float2 f = __half22float2(h2[q]);
+                                    ss = fmaf(f.x, f.x, ss);
+                                    ss = fmaf(f.y, f.y, ss);
+                                }
                             }
-                        *pb = qmin;
-                        *pi = (uint32_t)(bt * kNT + cq * kQC + c0 * 16) + j;
+                        }
+                        // fp16 inputs are bounded by 65504, so ss is finite unless an element is
+                        // Inf or NaN.
+                        finite = isfinite(ss);
+                        nu = finite ? sqrtf(ss) : 0.f;
+                        us = nu > 0.f ? (kOpScale / kPiScale) / nu : 0.f;     // 2^10 u = Y * us
+                    }
+                    uint32_t y[2][32];
+                    const uint32_t ycol = tmem_base + lane_off + buf * (uint32_t)kNT + (uint32_t)(pass * L::kPassCols);
+                    tmem_ld32_nowait(ycol, y[0]);
+                    tmem_ld32_nowait(ycol + 32, y[1]);
+                    tmem_wait_ld();
+                    const bool zero = !(nu > 0.f);
+#pragma unroll
+                    for (int j = 0; j < OWN; ++j) {
+                        const int bb = 2 * j + cq;
+                        float v[K];
+#pragma unroll
+                        for (int q = 0; q < K; ++q) {
+                            // bb is uniform over the warp; pick the columns with static indices.
+                            const int ce = (2 * j) * K + q, co = (2 * j + 1) * K + q;
+                            const float lo = __uint_as_float(y[ce / 32][ce % 32]);
+                            const float hi = __uint_as_float(y[co / 32][co % 32]);
+                            v[q] = zero ? 0.f : (cq ? hi : lo) * us;
+                        }
+                        uint32_t uh[K / 2], ul[K / 2];
+#pragma unroll
+                        for (int q = 0; q < K / 2; ++q) split_half2(v[2 * q], v[2 * q + 1], uh[q], ul[q]);
+                        const uint32_t one2 = 0x64006400u;            // (1024, 1024) in fp16
+                        uint8_t *arow = sm + L::oA + bb * L::kABlock + (t / 8) * (KP / 8) * 128 + (t % 8) * 16;
+                        if constexpr (K == 4) {
+                            *reinterpret_cast<uint4 *>(arow) = make_uint4(uh[0], uh[1], ul[0], ul[1]);
+                            *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(uh[0], uh[1], one2, 0u);
+                        } else {
+                            *reinterpret_cast<uint4 *>(arow) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+                            *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+                            *reinterpret_cast<uint4 *>(arow + 256) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
+                            *reinterpret_cast<uint4 *>(arow + 384) = make_uint4(one2, 0u, 0u, 0u);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    named_sync(1, kCons);
+                    if (tid == 0) {
+                        mbar_arrive(a_ready);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) mbar_arrive(freeb + buf);
+                        // The last pass's rotation was the x tile's last reader: fetch the next.
+                        const int64_t next = tile + gridDim.x;
+                        if (pass == NPASS - 1 && next < ntiles) {
+                            mbar_arrive_expect_tx(bar_x, (uint32_t)L::kXTile);
+#pragma unroll
+                            for (int kb = 0; kb < D / 64; ++kb)
+                                tma_load_2d(xt + kb * 16384, &xmap, kb * 64, (int)(next * kRows), bar_x);
+                        }
+                    }
+                    if (pass == NPASS - 1 && tile + gridDim.x < ntiles) ++x_issued;
+                    ++gi;
+                }
+                // --- score items ----------------------------------------------------------------
+                float best[OWN];
+                int chunk[OWN];
+#pragma unroll
+                for (int j = 0; j < OWN; ++j) {
+                    best[j] = INFINITY;
+                    chunk[j] = 0;
+                }
+#pragma unroll 1
+                for (int bt = 0; bt < nbt && ok; ++bt) {
+#pragma unroll
+                    for (int j = 0; j < OWN; ++j) {
+                        const uint32_t g = gi + (uint32_t)(bt * NBH + 2 * j + cq);
+                        const uint32_t buf = g % kBufs;
+                        const bool w = __all_sync(0xffffffffu, mbar_wait(ready + buf, (g / kBufs) & 1));
+                        if (!w) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        uint32_t sc[kNT / 32][32];
+                        const uint32_t col = tmem_base + lane_off + buf * (uint32_t)kNT;
+#pragma unroll
+                        for (int h = 0; h < kNT / 32; ++h) tmem_ld32_nowait(col + 32 * h, sc[h]);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(freeb + buf);      // the scores are in registers
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c) {
+                            float v16[16];
+#pragma unroll
+                            for (int z = 0; z < 16; ++z) v16[z] = __uint_as_float(sc[c / 2][16 * (c % 2) + z]);
+                            const float m = min16(v16);
+                            const bool better = m < best[j];
+                            best[j] = better ? m : best[j];
+                            chunk[j] = better ? bt * kChunks + c : chunk[j];
+                        }
                     }
                 }
+                gi += (uint32_t)(nbt * NBH);
                 ok = named_sync_and(1, kCons, ok);
                 if (!ok) break;
-                // Merge the four column quarters of each block (lowest score, then lowest index),
-                // pack, and free the state for the next pass.
-                if (cq == 0 && live) {
-                    for (int bb = 0; bb < NBH; ++bb) {
-                        float best = st_best[(bb * kCQ) * kRows + t];
-                        uint32_t bi = st_bi[(bb * kCQ) * kRows + t];
+                // --- resolution of the owned blocks' chunks, by squared difference ------------
+#pragma unroll 1
+                for (int j = 0; j < OWN; ++j) {
+                    const int bb = 2 * j + cq;
+                    const uint8_t *arow = sm + L::oA + bb * L::kABlock + (t / 8) * (KP / 8) * 128 + (t % 8) * 16;
+                    float u[K];
+                    if constexpr (K == 4) {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(arow);      // uh[4], ul[4]
+                        u[0] = (h2f_lo(a.x) + h2f_lo(a.z)) * (1.f / kOpScale);
+                        u[1] = (h2f_hi(a.x) + h2f_hi(a.z)) * (1.f / kOpScale);
+                        u[2] = (h2f_lo(a.y) + h2f_lo(a.w)) * (1.f / kOpScale);
+                        u[3] = (h2f_hi(a.y) + h2f_hi(a.w)) * (1.f / kOpScale);
+                    } else {
+                        const uint4 a = *reinterpret_cast<const uint4 *>(arow);         // uh[8]
+                        const uint4 b = *reinterpret_cast<const uint4 *>(arow + 128);   // ul[8]
+                        const uint32_t ah[4] = {a.x, a.y, a.z, a.w}, al[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                        for (int q = 1; q < kCQ; ++q) {
-                            const float v = st_best[(bb * kCQ + q) * kRows + t];
-                            const uint32_t n = st_bi[(bb * kCQ + q) * kRows + t];
-                            if (v < best || (v == best && n < bi)) {
-                                best = v;
-                                bi = n;
-                            }
+                        for (int q = 0; q < 4; ++q) {
+                            u[2 * q] = (h2f_lo(ah[q]) + h2f_lo(al[q])) * (1.f / kOpScale);
+                            u[2 * q + 1] = (h2f_hi(ah[q]) + h2f_hi(al[q])) * (1.f / kOpScale);
                         }
-                        wr.put(nu > 0.f ? bi : 0u, p.B);
                     }
+                    const int n0 = chunk[j] * kChunk;
+                    const float4 *cp = reinterpret_cast<const float4 *>(p.C + (size_t)n0 * K);
+                    float4 cw[kChunk * K / 4];
+#pragma unroll
+                    for (int q = 0; q < kChunk * K / 4; ++q) cw[q] = __ldg(cp + q);
+                    float bd = INFINITY;
+                    int bi = n0;
+#pragma unroll
+                    for (int q = 0; q < kChunk; ++q) {
+                        float dsum = 0.f;
+#pragma unroll
+                        for (int e = 0; e < K / 4; ++e) {
+                            const float4 c = cw[q * (K / 4) + e];
+                            const float e0 = u[4 * e] - c.x, e1 = u[4 * e + 1] - c.y;
+                            const float e2 = u[4 * e + 2] - c.z, e3 = u[4 * e + 3] - c.w;
+                            dsum = fmaf(e0, e0, dsum);
+                            dsum = fmaf(e1, e1, dsum);
+                            dsum = fmaf(e2, e2, dsum);
+                            dsum = fmaf(e3, e3, dsum);
+                        }
+                        if (dsum < bd) {
+                            bd = dsum;
+                            bi = n0 + q;
+                        }
+                    }
+                    idx_s[t * NB + pass * NBH + bb] = (uint16_t)bi;
                 }
-                ok = named_sync_and(1, kCons, true);
             }
             if (!ok) break;
+            named_sync(1, kCons);                     // every block's index is staged
             if (cq == 0 && live) {
+                const int64_t orow = p.map(r);
+                BitWriter wr(p.codes, orow * (int64_t)R);
+                const uint4 *row = reinterpret_cast<const uint4 *>(idx_s + t * NB);
+#pragma unroll
+                for (int w4 = 0; w4 < NB / 8; ++w4) {
+                    const uint4 v = row[w4];
+                    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        wr.put(nu > 0.f ? (ws[q] & 0xFFFFu) : 0u, p.B);
+                        wr.put(nu > 0.f ? (ws[q] >> 16) : 0u, p.B);
+                    }
+                }
                 wr.flush();
                 p.nu[orow] = nu;
                 if (!finite) atomicOr(p.flags, (uint32_t)FQ_FLAG_NONFINITE);
             }
         }
-        if (!ok && lead) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+        if (!ok && tid == 0) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+        // An x tile still in flight after a timeout lands before the CTA exits.
+        if (!ok && tid == 0 && x_issued > x_done) mbar_wait(bar_x, (x_issued - 1) & 1, 1000000ull);
     }
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem_base, L::kTmemCols);
+    if (warp == 0) tmem_dealloc(tmem_base, 512);
 }
 
-template <int D, int K, int NBH, int NT>
+template <int D, int K, int NBH>
 cudaError_t launch_kq(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu, uint32_t *codes,
                       cudaStream_t s) {
-    using L = KQ<D, K, NBH, NT>;
+    using L = KQ<D, K, NBH>;
     CUtensorMap tm;
     if (!encode_rows_tensor_map(&tm, x, M, D)) return cudaErrorInvalidValue;
     KQParams p;
@@ -420,29 +503,38 @@ cudaError_t launch_kq(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     p.B = ctx->B;
     p.pi_split = ctx->pi_split;
     p.cb_ops = ctx->cb_ops;
+    p.C = ctx->C;
     p.nu = nu;
     p.codes = codes;
     p.flags = ctx->flags;
     const int64_t ntiles = (M + kRows - 1) / kRows;
-    int64_t grid = ntiles < ctx->kq_max_ctas ? ntiles : ctx->kq_max_ctas;
-    encode_kq_tc<D, K, NBH, NT><<<(unsigned)grid, kThreads, L::kBytes, s>>>(tm, p);
-    return cudaGetLastError();
+    const int64_t grid = ntiles < ctx->kq_max_ctas ? ntiles : ctx->kq_max_ctas;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L::kBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, encode_kq_tc<D, K, NBH>, tm, p);
 }
 
-template <int D, int K, int NBH, int NT>
+template <int D, int K, int NBH>
 cudaError_t prep_kq(fq_ctx *ctx) {
-    using L = KQ<D, K, NBH, NT>;
-    static_assert(L::kBytes <= 227 * 1024, "shared memory budget");
+    using L = KQ<D, K, NBH>;
+    static_assert(L::kBytes <= kSmemBudget, "shared memory budget");
     static_assert(L::NB % NBH == 0, "passes");
-    cudaError_t e = cudaFuncSetAttribute(encode_kq_tc<D, K, NBH, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(encode_kq_tc<D, K, NBH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kBytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kq_tc<D, K, NBH, NT>, kThreads, L::kBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kq_tc<D, K, NBH>, kThreads, L::kBytes);
     if (e != cudaSuccess) return e;
-    // TMEM: each resident CTA holds kTmemCols of the SM's 512 columns.
-    const int by_tmem = 512 / (int)L::kTmemCols;
-    if (per_sm > by_tmem) per_sm = by_tmem;
+    // TMEM: each resident CTA holds all 512 columns of its SM.
+    if (per_sm > 1) per_sm = 1;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     ctx->kq_max_ctas = per_sm * ctx->num_sms;
     return cudaSuccess;
@@ -454,14 +546,14 @@ bool kq_tc_supported(const fq_ctx *ctx) {
     CUtensorMap probe;
     const bool shape = (ctx->d == 64 && ctx->k == 4) || (ctx->d == 128 && ctx->k == 8) ||
                        (ctx->d == 64 && ctx->k == 8) || (ctx->d == 128 && ctx->k == 4);
-    return shape && ctx->N >= 128 && ctx->N % 128 == 0 && ctx->N <= 65536 &&
+    return shape && ctx->N >= kNT && ctx->N % kNT == 0 && ctx->N <= 65536 &&
            encode_rows_tensor_map(&probe, ctx->Pi, 128, ctx->d);
 }
 
 // Codebook rows as B operands: [ch, ch, cl, hh, hl, 0...] per codeword (k-wide groups), in the
 // K-major no-swizzle layout: codeword n, 16-byte chunk kc of its row at
 // (n / 8) * (KP / 8) * 128 + kc * 128 + (n % 8) * 16, so any run of whole 8-codeword groups (a
-// 128- or 256-codeword tile) is contiguous.
+// 128-codeword tile) is contiguous.
 cudaError_t prepare_kq_tc(fq_ctx *ctx) {
     const int N = ctx->N, k = ctx->k, d = ctx->d;
     const int KP = (3 * k + 2 <= 16) ? 16 : 32;
@@ -506,18 +598,18 @@ cudaError_t prepare_kq_tc(fq_ctx *ctx) {
         if (e == cudaSuccess) e = cudaMemcpy(ctx->pi_split, pis.data(), pis.size() * 2, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return e;
     }
-    if (d == 64 && k == 4) return prep_kq<64, 4, 16, 128>(ctx);
-    if (d == 64 && k == 8) return prep_kq<64, 8, 8, 128>(ctx);
-    if (d == 128 && k == 4) return prep_kq<128, 4, 8, 128>(ctx);
-    return prep_kq<128, 8, 8, 128>(ctx);
+    if (d == 64 && k == 4) return prep_kq<64, 4, 16>(ctx);
+    if (d == 64 && k == 8) return prep_kq<64, 8, 8>(ctx);
+    if (d == 128 && k == 4) return prep_kq<128, 4, 16>(ctx);
+    return prep_kq<128, 8, 8>(ctx);
 }
 
 cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                 uint32_t *codes, cudaStream_t s) {
-    if (ctx->d == 64 && ctx->k == 4) return launch_kq<64, 4, 16, 128>(ctx, x, M, map, nu, codes, s);
-    if (ctx->d == 64 && ctx->k == 8) return launch_kq<64, 8, 8, 128>(ctx, x, M, map, nu, codes, s);
-    if (ctx->d == 128 && ctx->k == 4) return launch_kq<128, 4, 8, 128>(ctx, x, M, map, nu, codes, s);
-    return launch_kq<128, 8, 8, 128>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64 && ctx->k == 4) return launch_kq<64, 4, 16>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64 && ctx->k == 8) return launch_kq<64, 8, 8>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 128 && ctx->k == 4) return launch_kq<128, 4, 16>(ctx, x, M, map, nu, codes, s);
+    return launch_kq<128, 8, 8>(ctx, x, M, map, nu, codes, s);
 }
 
 }  // namespace fq

@@ -432,7 +432,11 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                             u[2 * q + 1] = (h2f_hi(ah[q]) + h2f_hi(al[q])) * (1.f / kOpScale);
                         }
                     }
-                    const int n0 = chunk[j] * kChunk;
+                    // chunk[] stays in registers only while every index into it is static.
+                    int cj = chunk[0];
+#pragma unroll
+                    for (int q = 1; q < OWN; ++q) cj = (q == j) ? chunk[q] : cj;
+                    const int n0 = cj * kChunk;
                     const float4 *cp = reinterpret_cast<const float4 *>(p.C + (size_t)n0 * K);
                     float4 cw[kChunk * K / 4];
 #pragma unroll

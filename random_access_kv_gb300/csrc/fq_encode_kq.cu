@@ -1,30 +1,41 @@
 // Tensor-core block encoder for k = 4 and k = 8 [FibQuant §2.3, encoder].
 //
-// Persistent CTAs, one per SM: 8 consumer warps (two per TMEM lane quarter), a loader warp (bulk
-// and TMA copies) and an MMA warp. For every 128-row tile of x, in passes of NBH blocks:
+// Persistent CTAs, one per SM: a loader warp (bulk and TMA copies), two MMA warps and 8 consumer
+// warps (two per TMEM lane quarter). Issuing tcgen05.mma costs the issuing thread about as much
+// time per instruction whatever the instruction's N, so the score MMAs take the widest N (256
+// codewords), two threads issue them (items alternate) and the issue loop is kept short
+// (descriptors built once, advanced by adds).
+// For every 128-row tile of x, in passes of NBH blocks:
 //   1. Rotation item: tcgen05.mma of the x tile (TMA, 128-byte swizzle) against fp16 hi/lo halves
-//      of 2^12 Pi into a TMEM buffer. Products of fp16 values are exact and the sums fp32, so Y
-//      carries fp32 accuracy. The consumers take nu from the shared-memory tile (first pass), read
-//      this pass's columns of Y and write one A-operand row per block b and row t:
-//          A_b = [uh, ul, uh, 2^10, 2^10, 0...],   uh + ul = fp16 hi/lo halves of 2^10 u_b,
+//      of 2^12 Pi, for the pass's columns of Y, into a TMEM buffer. Products of fp16 values are
+//      exact and the sums fp32, so Y carries fp32 accuracy. The consumers take nu from the
+//      shared-memory tile (first pass), read Y and write one A-operand row per block b and row t:
+//          A_b = [uh, ul, uh, 2^10, 2^10, sh, sl, 0...],   uh + ul = fp16 hi/lo halves of 2^10 u_b,
+//                                                         sh + sl = halves of 2^10 |u_b|^2,
 //      while every codeword n is a B-operand row
-//          B_n = [ch, ch, cl, hh, hl, 0...],        ch + cl = halves of 2^10 (-2 c_n),
-//                                                  hh + hl = halves of 2^10 |c_n|^2,
-//      so one MMA of K = 16 (k = 4) or K = 32 (k = 8) gives 2^20 (|c_n|^2 - 2 u_b.c_n) for 128
-//      rows and 128 codewords (the dropped ul*cl term is below 2^-22 of the result). This orders
-//      the codewords as |u_b - c_n|^2 does: the two differ by |u_b|^2, common to all n.
-//   2. Score items: for each 128-codeword tile of the codebook (resident in shared memory when
-//      it fits, else streamed through a ring) and each block of the pass, one MMA into one of
-//      four 128-column TMEM buffers. Consumer warp q (0 or 1) of a lane quarter takes the items
-//      of the blocks b = q mod 2: it reads its 32 rows x 128 scores, releases the buffer and
-//      folds the scores into a running (smallest score, 16-codeword chunk holding it) per (row,
-//      block): per chunk an 8-instruction tree of 3-input minima, one compare and two selects.
-//      Ties keep the earlier chunk.
-//   3. Resolution: at the end of the pass each (row, block) knows the chunk that holds its
-//      smallest tensor-core score. The 16 codewords of that chunk are scored again on the CUDA
+//          B_n = [ch, ch, cl, hh, hl, 2^10, 2^10, 0...],   ch + cl = halves of 2^10 (-2 c_n),
+//                                                         hh + hl = halves of 2^10 |c_n|^2,
+//      so one MMA of K = 16 (k = 4) or K = 32 (k = 8) gives 2^20 |u_b - c_n|^2 (as
+//      |c_n|^2 - 2 u_b.c_n + |u_b|^2) for 128 rows and NT codewords; the dropped ul*cl term is
+//      below 2^-22 of the terms. These scores are non-negative up to rounding.
+//   2. Score items: for each NT-codeword tile of the codebook (resident in shared memory when it
+//      fits, else streamed through a ring) and each block of the pass, one MMA into one of two
+//      NT-column TMEM buffers. The two consumer warps of a lane quarter read every item, each
+//      half of the columns (32 rows x 128 scores, in 16-column loads, the next load always in
+//      flight while the previous columns are folded), and release the buffer after their last
+//      load. A 16-column chunk folds to its minimum by a tree of 15 two-input minima (the min
+//      pipe's full rate); the chunk's number within the half goes into the three low mantissa
+//      bits (a relative change below 2^-20 of the score), so one integer minimum per chunk keeps
+//      the running (score, chunk) of the item and the lowest chunk wins a tie. Per (row, block)
+//      the best item so far and its codeword tile are kept (a later tile wins only by a lower key).
+//   3. Resolution: at the end of the pass the two halves' candidates of each (row, block) meet in
+//      shared memory (lower score, then lower codeword index), which gives the 16-codeword chunk
+//      that holds the smallest tensor-core score. Its 16 codewords are scored again on the CUDA
 //      cores by squared difference |u_b - c_n|^2 in fp32 (u_b = (uh + ul) / 2^10, the values the
-//      MMA used), lowest score first, ties to the lowest n. The codeword found is within twice
-//      the tensor-core scores' rounding (about 2^-22 of |c|^2 + 2|u.c|) of the true nearest one.
+//      MMA used), lowest score first, ties to the lowest n. The codeword found is within the
+//      tensor-core scores' rounding (about 2^-20 of the terms) of the true nearest one. The fp32
+//      codebook is read from shared memory: once u is in registers, the A operands' space takes
+//      it by bulk copies (as many rounds as it needs), so that these random reads never go to L2.
 //   4. Indices are staged in shared memory and packed at the record's fixed bit address; nu is
 //      stored.
 #include <cudaTypedefs.h>
@@ -44,45 +55,51 @@ namespace {
 using namespace sm100;
 
 constexpr int kRows = 128;
-constexpr int kNT = 128;                  // codewords per B tile (the MMA's N)
 constexpr int kChunk = 16;                // codewords per tracked chunk
-constexpr int kChunks = kNT / kChunk;     // chunks per item
-constexpr int kBufs = 4;                  // TMEM score buffers of kNT columns
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = kConsumerWarps * 32 + 64;      // + the loader warp and the MMA warp
+constexpr int kBufs = 2;                  // TMEM score buffers of NT columns
+constexpr int kQ = 2;                     // consumer warps per TMEM lane quarter (column parts of an item)
+constexpr int kConsumerWarps = 4 * kQ;
+constexpr int kLoaderWarp = kConsumerWarps, kMmaWarp0 = kConsumerWarps + 1;
+constexpr int kThreads = kConsumerWarps * 32 + 96;      // + the loader warp and two MMA warps
 constexpr uint32_t kCons = kConsumerWarps * 32;
 constexpr float kPiScale = 4096.f;        // 2^12 on Pi
 constexpr float kOpScale = 1024.f;        // 2^10 on u, -2c and |c|^2
 constexpr int kSmemBudget = 227 * 1024;
 
-template <int D, int K, int NBH>
+template <int D, int K, int NBH, int NT>
 struct KQ {
     static constexpr int NB = D / K;
     static constexpr int NPASS = NB / NBH;
     static constexpr int kPassCols = NBH * K;                     // Y columns one pass reads
-    static constexpr int KP = (3 * K + 2 <= 16) ? 16 : 32;        // padded K of one block's operand
+    static constexpr int KP = (3 * K + 4 <= 16) ? 16 : 32;        // padded K of one block's operand
     static constexpr int kPiPart = D * D * 2;
     static constexpr int kXTile = kRows * D * 2;
     static constexpr int kABlock = kRows * KP * 2;                // one block's A operand
-    static constexpr int kBTile = kNT * KP * 2;                   // one codebook tile
+    static constexpr int kBTile = NT * KP * 2;                    // one codebook tile
     static constexpr int oPi = 0;
     static constexpr int oX = oPi + 2 * kPiPart;
     static constexpr int oA = oX + kXTile;
+    static constexpr int kLd = NT / kQ;                           // score columns one consumer warp reads
     static constexpr int oIdx = oA + NBH * kABlock;               // uint16 [kRows][NB]
-    static constexpr int oRing = oIdx + ((kRows * NB * 2 + 1023) & ~1023);
+    static constexpr int oXch = oIdx + ((kRows * NB * 2 + 1023) & ~1023);   // [kQ][NBH][kRows] key, then tile
+    static constexpr int kXchBytes = (kQ * NBH * kRows * 6 + 1023) & ~1023;
+    static constexpr int oRing = oXch + kXchBytes;
     static constexpr int kTail = 512 + 16 + 1024;                 // barriers, TMEM slot, alignment slack
     static constexpr int kStagesFit = (kSmemBudget - oRing - kTail) / kBTile;
     static constexpr int kStages = kStagesFit > 16 ? 16 : kStagesFit;
     static constexpr int oBar = oRing + kStages * kBTile;
-    // bars: pi, x, a_ready, drain, ready[kBufs], freeb[kBufs], full[kStages], empty[kStages]
-    static constexpr int kBars = 4 + 2 * kBufs + 2 * kStages;
+    // bars: pi, x, a_ready, res, drain[2], ready[kBufs], freeb[kBufs], full[kStages], empty[kStages]
+    static constexpr int kBars = 6 + 2 * kBufs + 2 * kStages;
+    static constexpr int kResCw = NBH * kABlock / (K * 4);         // fp32 codewords the A space holds
     static constexpr int oTmem = oBar + kBars * 8;
     static constexpr int kBytes = oTmem + 16 + 1024;
     static_assert(kStages >= 2, "codebook ring");
     static_assert(kBars * 8 <= 512, "barrier space");
-    static_assert(kPassCols == 64, "one pass reads 64 columns of Y");
-    static_assert(D <= kNT, "the rotation fits one score buffer");
-    static_assert(NBH % 2 == 0, "two consumer warps alternate over the blocks");
+    static_assert(kPassCols % 32 == 0 && kPassCols <= 64, "one pass reads 32 or 64 columns of Y");
+    static_assert(kBufs * NT <= 512, "tensor memory");
+    static_assert(kLd % 32 == 0 && kPassCols <= NT, "score buffers: 16-column loads, an even number per consumer warp and item");
+    static_assert(kResCw % kChunk == 0, "resolution rounds hold whole chunks");
+    static_assert(NBH % kQ == 0, "the consumer warps of a lane quarter split the blocks' A rows");
 };
 
 struct KQParams {
@@ -90,7 +107,7 @@ struct KQParams {
     RowMap map;
     int N, B;
     const uint8_t *pi_split;   // fp16 halves of 2^12 Pi, swizzled (as the k = 2 encoder)
-    const uint8_t *cb_ops;     // [N / kNT] tiles of B rows, no-swizzle K-major core-matrix layout
+    const uint8_t *cb_ops;     // [N / NT] tiles of B rows, no-swizzle K-major core-matrix layout
     const float *C;            // [N x K] fp32 codebook (chunk resolution)
     float *nu;
     uint32_t *codes;
@@ -111,19 +128,21 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_noswz(uint32_t saddr, uint32_t 
 __device__ __forceinline__ float h2f_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
 __device__ __forceinline__ float h2f_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
-template <int D, int K, int NBH>
+template <int D, int K, int NBH, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
 encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
-    using L = KQ<D, K, NBH>;
+    using L = KQ<D, K, NBH, NT>;
     constexpr int KP = L::KP, NB = L::NB, NPASS = L::NPASS, S = L::kStages;
-    constexpr int OWN = NBH / 2;                       // blocks of a pass one consumer warp owns
+    constexpr int OWN = NBH / kQ;                      // blocks of a pass whose A rows one consumer warp writes
+    constexpr uint32_t kSubMask = (uint32_t)(L::kLd / kChunk) - 1u;   // key bits that carry the chunk within a part
+    constexpr int kLd = L::kLd;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
-    uint64_t *bar_pi = bars + 0, *bar_x = bars + 1, *a_ready = bars + 2, *drain = bars + 3;
-    uint64_t *ready = bars + 4, *freeb = bars + 4 + kBufs;
-    uint64_t *full = bars + 4 + 2 * kBufs, *empty = bars + 4 + 2 * kBufs + S;
+    uint64_t *bar_pi = bars + 0, *bar_x = bars + 1, *a_ready = bars + 2, *res_bar = bars + 3, *drain = bars + 4;
+    uint64_t *ready = bars + 6, *freeb = bars + 6 + kBufs;
+    uint64_t *full = bars + 6 + 2 * kBufs, *empty = bars + 6 + 2 * kBufs + S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
     uint8_t *xt = sm + L::oX;
     uint8_t *ring = sm + L::oRing;
@@ -133,21 +152,23 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
     const int warp = tid / 32;
     const int lane = tid & 31;
     const int64_t ntiles = (p.M + kRows - 1) / kRows;
-    const int nbt = p.N / kNT;
+    const int nbt = p.N / NT;
     const bool resident = nbt <= S;                   // the whole codebook fits the ring
 
     if (tid == 0) {
         mbar_init(bar_pi, 1);
         mbar_init(bar_x, 1);
         mbar_init(a_ready, 1);
+        mbar_init(res_bar, 1);
         mbar_init(drain, 1);
+        mbar_init(drain + 1, 1);
         for (int b = 0; b < kBufs; ++b) {
             mbar_init(ready + b, 1);
-            mbar_init(freeb + b, 4);                  // one warp per lane quarter reads an item
+            mbar_init(freeb + b, kConsumerWarps);     // every consumer warp reads its part of an item
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, 2);                  // both MMA warps' items on the stage are done
         }
         fence_barrier_init();
     }
@@ -159,7 +180,7 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
     // touches memory this one writes.
     griddep_launch_dependents();
 
-    if (warp == kConsumerWarps) {
+    if (warp == kLoaderWarp) {
         // Loader: Pi and (when resident) the whole codebook, then the first x tile, then the
         // codebook tiles in the order the MMA warp uses them.
         if (lane == 0) {
@@ -199,38 +220,48 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                 mbar_wait(full + s, (n_s - 1) & 1, ok ? 2000000000ull : 1000000ull);
             }
         }
-    } else if (warp == kConsumerWarps + 1) {
-        // MMA issuer: per pass a rotation item, then the score items in (tile, block) order.
+    } else if (warp >= kMmaWarp0) {
+        // MMA issuers: per pass a rotation item, then the score items in (codeword tile, block)
+        // order; item n goes to buffer n mod 2 and is issued by MMA warp n mod 2.
+        const uint32_t q = (uint32_t)(warp - kMmaWarp0);
         if (lane == 0) {
-            const uint32_t idesc_rot = idesc_f16_f32(128, D);
-            const uint32_t idesc_sc = idesc_f16_f32(128, kNT);
+            const uint32_t idesc_rot = idesc_f16_f32(128, L::kPassCols);
+            const uint32_t idesc_sc = idesc_f16_f32(128, NT);
             const uint32_t pi_hi = smem_addr(sm + L::oPi), pi_lo = pi_hi + L::kPiPart;
-            const uint32_t a_base = smem_addr(sm + L::oA), b_base = smem_addr(ring);
+            const uint64_t da0 = sdesc_kmajor_noswz(smem_addr(sm + L::oA), (KP / 8) * 128);
+            const uint64_t db0 = sdesc_kmajor_noswz(smem_addr(ring), (KP / 8) * 128);
+            constexpr uint32_t kStepK = 256u >> 4;    // the next 16 K elements: two 128-byte core columns
+            constexpr uint32_t kAStep = (uint32_t)L::kABlock >> 4, kBStep = (uint32_t)L::kBTile >> 4;
             bool ok = mbar_wait(bar_pi, 0);
-            uint32_t gi = 0, k = 0, npass = 0;
+            uint32_t n = 0;                           // items issued
+            uint32_t k = 0, npass = 0;
             int64_t it = 0;
             for (int64_t tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x, ++it) {
                 for (int pass = 0; pass < NPASS && ok; ++pass, ++npass) {
-                    uint32_t buf = gi % kBufs;
-                    if (gi >= kBufs) ok = mbar_wait(freeb + buf, (gi / kBufs - 1) & 1);
-                    if (ok && pass == 0) ok = mbar_wait(bar_x, (uint32_t)(it & 1));
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t xa = smem_addr(xt);
-                    const uint32_t rot = tmem_base + buf * (uint32_t)kNT;
+                    if ((n & 1u) == q) {
+                        const uint32_t buf = n & 1u, use = n >> 1;
+                        if (use > 0) ok = mbar_wait(freeb + buf, (use - 1) & 1);
+                        if (ok && pass == 0) ok = mbar_wait(bar_x, (uint32_t)(it & 1));
+                        if (!ok) break;
+                        tc_fence_after();
+                        // Y[:, pass*64 .. +64) = X Pi[pass*64 .. +64, :]^T: the B rows of this pass.
+                        const uint32_t xa = smem_addr(xt);
+                        const uint32_t rot = tmem_base + buf * (uint32_t)NT;
+                        const uint32_t prow = (uint32_t)(pass * L::kPassCols * 128);
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t pb = half ? pi_lo : pi_hi;
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t pb = (half ? pi_lo : pi_hi) + prow;
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t koff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                            const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
-                            mma_f16(rot, sdesc_sw128(xa + koff), sdesc_sw128(pb + boff), idesc_rot,
-                                    (half | kk) ? 1u : 0u);
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t koff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
+                                const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
+                                mma_f16(rot, sdesc_sw128(xa + koff), sdesc_sw128(pb + boff), idesc_rot,
+                                        (half | kk) ? 1u : 0u);
+                            }
                         }
+                        mma_commit(ready + buf);
                     }
-                    mma_commit(ready + buf);
-                    ++gi;
+                    ++n;
                     // The consumers have written this pass's A operands (and read the rotation).
                     ok = mbar_wait(a_ready, npass & 1);
                     if (!ok) break;
@@ -238,20 +269,24 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     for (int bt = 0; bt < nbt && ok; ++bt) {
                         const uint32_t s = resident ? (uint32_t)bt : k % S;
                         ok = mbar_wait(full + s, resident ? 0u : (k / S) & 1);
-                        for (int bb = 0; bb < NBH && ok; ++bb) {
-                            buf = gi % kBufs;
-                            if (gi >= kBufs) ok = mbar_wait(freeb + buf, (gi / kBufs - 1) & 1);
+                        const uint64_t db = db0 + (uint64_t)(s * kBStep);
+                        uint64_t da = da0;
+                        // This warp's items of the tile: blocks bb with (n + bb) mod 2 = q.
+                        const uint32_t b0 = (n & 1u) ^ q;
+                        n += (uint32_t)NBH;
+                        da += b0 * kAStep;
+#pragma unroll 1
+                        for (uint32_t bb = b0; bb < (uint32_t)NBH && ok; bb += 2, da += 2 * kAStep) {
+                            const uint32_t g = n - (uint32_t)NBH + bb;
+                            const uint32_t buf = g & 1u, use = g >> 1;
+                            if (use > 0) ok = mbar_wait(freeb + buf, (use - 1) & 1);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint32_t aa = a_base + (uint32_t)(bb * L::kABlock);
-                            const uint32_t ba = b_base + s * (uint32_t)L::kBTile;
-                            const uint32_t dst = tmem_base + buf * (uint32_t)kNT;
+                            const uint32_t dst = tmem_base + buf * (uint32_t)NT;
+                            mma_f16(dst, da, db, idesc_sc, 0u);
 #pragma unroll
-                            for (int kk = 0; kk < KP / 16; ++kk)
-                                mma_f16(dst, sdesc_kmajor_noswz(aa + kk * 256, (KP / 8) * 128),
-                                        sdesc_kmajor_noswz(ba + kk * 256, (KP / 8) * 128), idesc_sc, kk ? 1u : 0u);
+                            for (int kk = 1; kk < KP / 16; ++kk) mma_f16(dst, da + kk * kStepK, db + kk * kStepK, idesc_sc, 1u);
                             mma_commit(ready + buf);
-                            ++gi;
                         }
                         if (!resident) {
                             if (ok) mma_commit(empty + s);
@@ -262,18 +297,19 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
             }
             if (!ok) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
             // Every MMA issued has completed before the CTA can exit.
-            mma_commit(drain);
-            mbar_wait(drain, 0, ok ? 2000000000ull : 1000000ull);
+            mma_commit(drain + q);
+            mbar_wait(drain + q, 0, ok ? 2000000000ull : 1000000ull);
         }
     } else {
-        // Consumers: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. rows t of the tile, and owns
-        // the blocks b = w / 4 (mod 2) of every pass.
+        // Consumers: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. rows t of the tile; it reads
+        // column part w / 4 of every item and writes (and resolves) the blocks b = w / 4 (mod kQ).
         const int lq = warp % 4, cq = warp / 4;
         const int t = 32 * lq + lane;
         const uint32_t lane_off = (uint32_t)(32 * lq) << 16;
         const int R = NB * p.B;
         griddep_wait();                               // the code store may be the previous kernel's
-        uint32_t gi = 0;
+        uint32_t n = 0;                               // items of the MMA warps' sequence passed
+        uint32_t res_n = 0;                           // codebook rounds copied for the resolution
         bool ok = true;
         int64_t it = 0;
         uint32_t x_issued = (int64_t)blockIdx.x < ntiles ? 1u : 0u, x_done = 0;
@@ -285,8 +321,8 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
             for (int pass = 0; pass < NPASS && ok; ++pass) {
                 // --- rotation item: nu (first pass), then this pass's A operands ---------------
                 {
-                    const uint32_t buf = gi % kBufs;
-                    bool w = mbar_wait(ready + buf, (gi / kBufs) & 1);
+                    const uint32_t buf = n & 1u;
+                    bool w = mbar_wait(ready + buf, (n >> 1) & 1);
                     if (pass == 0) w = w && mbar_wait(bar_x, (uint32_t)(it & 1));
                     ok = named_sync_and(1, kCons, w);
                     if (!ok) break;
@@ -302,8 +338,8 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                                     *reinterpret_cast<const uint4 *>(xt + kb * 16384 + t * 128 + ((c ^ (t & 7)) << 4));
                                 const __half2 *h2 = reinterpret_cast<const __half2 *>(&v);
 #pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const float2 f = __half22float2(h2[q]);
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = __half22float2(h2[e]);
                                     ss = fmaf(f.x, f.x, ss);
                                     ss = fmaf(f.y, f.y, ss);
                                 }
@@ -315,37 +351,49 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                         nu = finite ? sqrtf(ss) : 0.f;
                         us = nu > 0.f ? (kOpScale / kPiScale) / nu : 0.f;     // 2^10 u = Y * us
                     }
-                    uint32_t y[2][32];
-                    const uint32_t ycol = tmem_base + lane_off + buf * (uint32_t)kNT + (uint32_t)(pass * L::kPassCols);
-                    tmem_ld32_nowait(ycol, y[0]);
-                    tmem_ld32_nowait(ycol + 32, y[1]);
+                    // This warp's blocks' columns of Y (the column address is per warp, so each
+                    // block's K columns are one load).
+                    uint32_t y[OWN][K];
+                    const uint32_t ycol = tmem_base + lane_off + buf * (uint32_t)NT;
+#pragma unroll
+                    for (int j = 0; j < OWN; ++j) {
+                        const uint32_t ca = ycol + (uint32_t)((kQ * j + cq) * K);
+                        if constexpr (K == 4) tmem_ld4_nowait(ca, y[j]);
+                        else tmem_ld8_nowait(ca, y[j]);
+                    }
                     tmem_wait_ld();
                     const bool zero = !(nu > 0.f);
 #pragma unroll
                     for (int j = 0; j < OWN; ++j) {
-                        const int bb = 2 * j + cq;
+                        const int bb = kQ * j + cq;
                         float v[K];
+                        float uu = 0.f;
 #pragma unroll
-                        for (int q = 0; q < K; ++q) {
-                            // bb is uniform over the warp; pick the columns with static indices.
-                            const int ce = (2 * j) * K + q, co = (2 * j + 1) * K + q;
-                            const float lo = __uint_as_float(y[ce / 32][ce % 32]);
-                            const float hi = __uint_as_float(y[co / 32][co % 32]);
-                            v[q] = zero ? 0.f : (cq ? hi : lo) * us;
+                        for (int e = 0; e < K; ++e) {
+                            v[e] = zero ? 0.f : __uint_as_float(y[j][e]) * us;
+                            uu = fmaf(v[e], v[e], uu);
                         }
-                        uint32_t uh[K / 2], ul[K / 2];
+                        uint32_t uh[K / 2], ul[K / 2], ss2, sdummy;
 #pragma unroll
-                        for (int q = 0; q < K / 2; ++q) split_half2(v[2 * q], v[2 * q + 1], uh[q], ul[q]);
+                        for (int e = 0; e < K / 2; ++e) split_half2(v[2 * e], v[2 * e + 1], uh[e], ul[e]);
+                        // 2^10 |u_b|^2 = sum (2^10 u)^2 / 2^10 as fp16 hi/lo, packed (hi, lo)
+                        {
+                            const float su = uu * (1.f / kOpScale);
+                            const __half sh = __float2half_rn(su);
+                            const __half sl = __float2half_rn(su - __half2float(sh));
+                            ss2 = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(sl) << 16);
+                            sdummy = 0u;
+                        }
                         const uint32_t one2 = 0x64006400u;            // (1024, 1024) in fp16
                         uint8_t *arow = sm + L::oA + bb * L::kABlock + (t / 8) * (KP / 8) * 128 + (t % 8) * 16;
                         if constexpr (K == 4) {
                             *reinterpret_cast<uint4 *>(arow) = make_uint4(uh[0], uh[1], ul[0], ul[1]);
-                            *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(uh[0], uh[1], one2, 0u);
+                            *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(uh[0], uh[1], one2, ss2);
                         } else {
                             *reinterpret_cast<uint4 *>(arow) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
                             *reinterpret_cast<uint4 *>(arow + 128) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
                             *reinterpret_cast<uint4 *>(arow + 256) = make_uint4(uh[0], uh[1], uh[2], uh[3]);
-                            *reinterpret_cast<uint4 *>(arow + 384) = make_uint4(one2, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4 *>(arow + 384) = make_uint4(one2, ss2, sdummy, 0u);
                         }
                     }
                     fence_proxy_async_smem();
@@ -354,7 +402,7 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     if (tid == 0) {
                         mbar_arrive(a_ready);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) mbar_arrive(freeb + buf);
+                        for (int e = 0; e < kConsumerWarps; ++e) mbar_arrive(freeb + buf);
                         // The last pass's rotation was the x tile's last reader: fetch the next.
                         const int64_t next = tile + gridDim.x;
                         if (pass == NPASS - 1 && next < ntiles) {
@@ -365,104 +413,177 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                         }
                     }
                     if (pass == NPASS - 1 && tile + gridDim.x < ntiles) ++x_issued;
-                    ++gi;
+                    ++n;
                 }
-                // --- score items ----------------------------------------------------------------
-                float best[OWN];
-                int chunk[OWN];
+                // --- score items: this warp's part of the columns of every item --------------------
+                // Loads of 16 columns; the next load is always in flight while the previous 16
+                // columns are folded (tcgen05.wait::ld waits for all loads issued so far, and at each
+                // wait only the newest is outstanding).
+                int bkey[NBH], btile[NBH];
 #pragma unroll
-                for (int j = 0; j < OWN; ++j) {
-                    best[j] = INFINITY;
-                    chunk[j] = 0;
+                for (int bb = 0; bb < NBH; ++bb) {
+                    bkey[bb] = 0x7FFFFFFF;
+                    btile[bb] = 0;
+                }
+                uint32_t rr[2][16];
+                const uint32_t colq = tmem_base + lane_off + (uint32_t)(cq * kLd);
+                // The first item's first 16 columns.
+                {
+                    const uint32_t buf = n & 1u;
+                    ok = __all_sync(0xffffffffu, mbar_wait(ready + buf, (n >> 1) & 1));
+                    if (ok) {
+                        tc_fence_after();
+                        tmem_ld16_nowait(colq + buf * (uint32_t)NT, rr[0]);
+                        tmem_wait_ld();
+                    }
                 }
 #pragma unroll 1
                 for (int bt = 0; bt < nbt && ok; ++bt) {
 #pragma unroll
-                    for (int j = 0; j < OWN; ++j) {
-                        const uint32_t g = gi + (uint32_t)(bt * NBH + 2 * j + cq);
-                        const uint32_t buf = g % kBufs;
-                        const bool w = __all_sync(0xffffffffu, mbar_wait(ready + buf, (g / kBufs) & 1));
-                        if (!w) {
-                            ok = false;
-                            break;
+                    for (int bb = 0; bb < NBH; ++bb) {
+                        const uint32_t g = n + (uint32_t)(bt * NBH + bb);
+                        const uint32_t buf = g & 1u;
+                        const uint32_t col = colq + buf * (uint32_t)NT;
+                        const bool more = bb + 1 < NBH || bt + 1 < nbt;
+                        int ikey = 0x7FFFFFFF;
+#pragma unroll
+                        for (int sub = 0; sub < kLd / 16; ++sub) {
+                            const int cur = sub & 1, nxt = cur ^ 1;
+                            if (sub + 1 < kLd / 16) {
+                                tmem_ld16_nowait(col + 16 * (sub + 1), rr[nxt]);
+                            } else if (more) {
+                                // the next item's first 16 columns
+                                const uint32_t gn = g + 1, bn = gn & 1u;
+                                ok = __all_sync(0xffffffffu, mbar_wait(ready + bn, (gn >> 1) & 1));
+                                if (ok) {
+                                    tc_fence_after();
+                                    tmem_ld16_nowait(colq + bn * (uint32_t)NT, rr[nxt]);
+                                }
+                            }
+                            float v[16];
+#pragma unroll
+                            for (int z = 0; z < 16; ++z) v[z] = __uint_as_float(rr[cur][z]);
+#pragma unroll
+                            for (int wd = 8; wd > 0; wd /= 2)
+#pragma unroll
+                                for (int z = 0; z < wd; ++z) v[z] = fminf(v[z], v[z + wd]);
+                            ikey = min(ikey, (int)((__float_as_uint(v[0]) & ~kSubMask) | (uint32_t)sub));
+                            if (sub + 1 < kLd / 16 || more) tmem_wait_ld();
+                            if (sub + 2 == kLd / 16) {
+                                // the item's last load has landed (waited just above): release the buffer
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(freeb + buf);
+                            }
                         }
-                        tc_fence_after();
-                        uint32_t sc[kNT / 32][32];
-                        const uint32_t col = tmem_base + lane_off + buf * (uint32_t)kNT;
-#pragma unroll
-                        for (int h = 0; h < kNT / 32; ++h) tmem_ld32_nowait(col + 32 * h, sc[h]);
-                        tmem_wait_ld();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(freeb + buf);      // the scores are in registers
-#pragma unroll
-                        for (int c = 0; c < kChunks; ++c) {
-                            float v16[16];
-#pragma unroll
-                            for (int z = 0; z < 16; ++z) v16[z] = __uint_as_float(sc[c / 2][16 * (c % 2) + z]);
-                            const float m = min16(v16);
-                            const bool better = m < best[j];
-                            best[j] = better ? m : best[j];
-                            chunk[j] = better ? bt * kChunks + c : chunk[j];
-                        }
+                        const bool better = ikey < bkey[bb];
+                        bkey[bb] = better ? ikey : bkey[bb];
+                        btile[bb] = better ? bt : btile[bb];
+                        if (!ok) break;
                     }
                 }
-                gi += (uint32_t)(nbt * NBH);
+                n += (uint32_t)(nbt * NBH);
+                // Candidates of the column parts to shared memory: the resolver of a block takes all.
+                int *xk = reinterpret_cast<int *>(sm + L::oXch);
+                uint16_t *xt16 = reinterpret_cast<uint16_t *>(sm + L::oXch + kQ * NBH * kRows * 4);
+#pragma unroll
+                for (int bb = 0; bb < NBH; ++bb) {
+                    xk[(cq * NBH + bb) * kRows + t] = bkey[bb];
+                    xt16[(cq * NBH + bb) * kRows + t] = (uint16_t)btile[bb];
+                }
                 ok = named_sync_and(1, kCons, ok);
                 if (!ok) break;
                 // --- resolution of the owned blocks' chunks, by squared difference ------------
-#pragma unroll 1
+                // u of the owned blocks into registers (from the A rows: the values the MMA used),
+                // and the winning chunk of each: the lowest score part of the parts' keys, then the
+                // lowest codeword index (tile, part, chunk within the part).
+                float u[OWN][K];
+                int cjs[OWN];
+#pragma unroll
                 for (int j = 0; j < OWN; ++j) {
-                    const int bb = 2 * j + cq;
+                    const int bb = kQ * j + cq;
                     const uint8_t *arow = sm + L::oA + bb * L::kABlock + (t / 8) * (KP / 8) * 128 + (t % 8) * 16;
-                    float u[K];
                     if constexpr (K == 4) {
                         const uint4 a = *reinterpret_cast<const uint4 *>(arow);      // uh[4], ul[4]
-                        u[0] = (h2f_lo(a.x) + h2f_lo(a.z)) * (1.f / kOpScale);
-                        u[1] = (h2f_hi(a.x) + h2f_hi(a.z)) * (1.f / kOpScale);
-                        u[2] = (h2f_lo(a.y) + h2f_lo(a.w)) * (1.f / kOpScale);
-                        u[3] = (h2f_hi(a.y) + h2f_hi(a.w)) * (1.f / kOpScale);
+                        u[j][0] = (h2f_lo(a.x) + h2f_lo(a.z)) * (1.f / kOpScale);
+                        u[j][1] = (h2f_hi(a.x) + h2f_hi(a.z)) * (1.f / kOpScale);
+                        u[j][2] = (h2f_lo(a.y) + h2f_lo(a.w)) * (1.f / kOpScale);
+                        u[j][3] = (h2f_hi(a.y) + h2f_hi(a.w)) * (1.f / kOpScale);
                     } else {
                         const uint4 a = *reinterpret_cast<const uint4 *>(arow);         // uh[8]
                         const uint4 b = *reinterpret_cast<const uint4 *>(arow + 128);   // ul[8]
                         const uint32_t ah[4] = {a.x, a.y, a.z, a.w}, al[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            u[2 * q] = (h2f_lo(ah[q]) + h2f_lo(al[q])) * (1.f / kOpScale);
-                            u[2 * q + 1] = (h2f_hi(ah[q]) + h2f_hi(al[q])) * (1.f / kOpScale);
+                        for (int e = 0; e < 4; ++e) {
+                            u[j][2 * e] = (h2f_lo(ah[e]) + h2f_lo(al[e])) * (1.f / kOpScale);
+                            u[j][2 * e + 1] = (h2f_hi(ah[e]) + h2f_hi(al[e])) * (1.f / kOpScale);
                         }
                     }
-                    // chunk[] stays in registers only while every index into it is static.
-                    int cj = chunk[0];
+                    int bs = 0x7FFFFFFF, bc = 0;
 #pragma unroll
-                    for (int q = 1; q < OWN; ++q) cj = (q == j) ? chunk[q] : cj;
-                    const int n0 = cj * kChunk;
-                    const float4 *cp = reinterpret_cast<const float4 *>(p.C + (size_t)n0 * K);
-                    float4 cw[kChunk * K / 4];
-#pragma unroll
-                    for (int q = 0; q < kChunk * K / 4; ++q) cw[q] = __ldg(cp + q);
-                    float bd = INFINITY;
-                    int bi = n0;
-#pragma unroll
-                    for (int q = 0; q < kChunk; ++q) {
-                        float dsum = 0.f;
-#pragma unroll
-                        for (int e = 0; e < K / 4; ++e) {
-                            const float4 c = cw[q * (K / 4) + e];
-                            const float e0 = u[4 * e] - c.x, e1 = u[4 * e + 1] - c.y;
-                            const float e2 = u[4 * e + 2] - c.z, e3 = u[4 * e + 3] - c.w;
-                            dsum = fmaf(e0, e0, dsum);
-                            dsum = fmaf(e1, e1, dsum);
-                            dsum = fmaf(e2, e2, dsum);
-                            dsum = fmaf(e3, e3, dsum);
-                        }
-                        if (dsum < bd) {
-                            bd = dsum;
-                            bi = n0 + q;
+                    for (int q = 0; q < kQ; ++q) {
+                        const int key = xk[(q * NBH + bb) * kRows + t];
+                        const int sc = key & ~(int)kSubMask;
+                        const int cidx = (int)xt16[(q * NBH + bb) * kRows + t] * (NT / kChunk) + q * (kLd / kChunk) +
+                                         (key & (int)kSubMask);
+                        if (sc < bs || (sc == bs && cidx < bc)) {
+                            bs = sc;
+                            bc = cidx;
                         }
                     }
-                    idx_s[t * NB + pass * NBH + bb] = (uint16_t)bi;
+                    cjs[j] = bc;
                 }
+                // The A space is free once every consumer holds its u: it takes the fp32 codebook,
+                // L::kResCw codewords per round.
+                fence_proxy_async_smem();
+                named_sync(1, kCons);
+                float bd[OWN];
+                int bi[OWN];
+#pragma unroll
+                for (int j = 0; j < OWN; ++j) {
+                    bd[j] = INFINITY;
+                    bi[j] = cjs[j] * kChunk;
+                }
+                const float *cs = reinterpret_cast<const float *>(sm + L::oA);
+#pragma unroll 1
+                for (int base = 0; base < p.N && ok; base += L::kResCw) {
+                    const int ncw = p.N - base < L::kResCw ? p.N - base : L::kResCw;
+                    if (tid == 0) {
+                        mbar_arrive_expect_tx(res_bar, (uint32_t)(ncw * K * 4));
+                        bulk_g2s(sm + L::oA, p.C + (size_t)base * K, (uint32_t)(ncw * K * 4), res_bar);
+                    }
+                    ok = named_sync_and(1, kCons, mbar_wait(res_bar, res_n & 1));
+                    ++res_n;
+                    if (!ok) break;
+#pragma unroll
+                    for (int j = 0; j < OWN; ++j) {
+                        const int c0 = cjs[j] * kChunk - base;
+                        if (c0 >= 0 && c0 < ncw) {
+#pragma unroll 4
+                            for (int q = 0; q < kChunk; ++q) {
+                                const float4 *cp = reinterpret_cast<const float4 *>(cs + (size_t)(c0 + q) * K);
+                                float dsum = 0.f;
+#pragma unroll
+                                for (int e = 0; e < K / 4; ++e) {
+                                    const float4 c = cp[e];
+                                    const float e0 = u[j][4 * e] - c.x, e1 = u[j][4 * e + 1] - c.y;
+                                    const float e2 = u[j][4 * e + 2] - c.z, e3 = u[j][4 * e + 3] - c.w;
+                                    dsum = fmaf(e0, e0, dsum);
+                                    dsum = fmaf(e1, e1, dsum);
+                                    dsum = fmaf(e2, e2, dsum);
+                                    dsum = fmaf(e3, e3, dsum);
+                                }
+                                if (dsum < bd[j]) {
+                                    bd[j] = dsum;
+                                    bi[j] = base + c0 + q;
+                                }
+                            }
+                        }
+                    }
+                    named_sync(1, kCons);             // every read of this round is done
+                }
+#pragma unroll
+                for (int j = 0; j < OWN; ++j) idx_s[t * NB + pass * NBH + kQ * j + cq] = (uint16_t)bi[j];
             }
             if (!ok) break;
             named_sync(1, kCons);                     // every block's index is staged
@@ -494,10 +615,10 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
     if (warp == 0) tmem_dealloc(tmem_base, 512);
 }
 
-template <int D, int K, int NBH>
+template <int D, int K, int NBH, int NT>
 cudaError_t launch_kq(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu, uint32_t *codes,
                       cudaStream_t s) {
-    using L = KQ<D, K, NBH>;
+    using L = KQ<D, K, NBH, NT>;
     CUtensorMap tm;
     if (!encode_rows_tensor_map(&tm, x, M, D)) return cudaErrorInvalidValue;
     KQParams p;
@@ -523,19 +644,19 @@ cudaError_t launch_kq(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, encode_kq_tc<D, K, NBH>, tm, p);
+    return cudaLaunchKernelEx(&cfg, encode_kq_tc<D, K, NBH, NT>, tm, p);
 }
 
-template <int D, int K, int NBH>
+template <int D, int K, int NBH, int NT>
 cudaError_t prep_kq(fq_ctx *ctx) {
-    using L = KQ<D, K, NBH>;
+    using L = KQ<D, K, NBH, NT>;
     static_assert(L::kBytes <= kSmemBudget, "shared memory budget");
     static_assert(L::NB % NBH == 0, "passes");
-    cudaError_t e = cudaFuncSetAttribute(encode_kq_tc<D, K, NBH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(encode_kq_tc<D, K, NBH, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kBytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kq_tc<D, K, NBH>, kThreads, L::kBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kq_tc<D, K, NBH, NT>, kThreads, L::kBytes);
     if (e != cudaSuccess) return e;
     // TMEM: each resident CTA holds all 512 columns of its SM.
     if (per_sm > 1) per_sm = 1;
@@ -550,17 +671,17 @@ bool kq_tc_supported(const fq_ctx *ctx) {
     CUtensorMap probe;
     const bool shape = (ctx->d == 64 && ctx->k == 4) || (ctx->d == 128 && ctx->k == 8) ||
                        (ctx->d == 64 && ctx->k == 8) || (ctx->d == 128 && ctx->k == 4);
-    return shape && ctx->N >= kNT && ctx->N % kNT == 0 && ctx->N <= 65536 &&
+    return shape && ctx->N >= 256 && ctx->N % 256 == 0 && ctx->N <= 65536 &&
            encode_rows_tensor_map(&probe, ctx->Pi, 128, ctx->d);
 }
 
-// Codebook rows as B operands: [ch, ch, cl, hh, hl, 0...] per codeword (k-wide groups), in the
+// Codebook rows as B operands: [ch, ch, cl, hh, hl, 2^10, 2^10, 0...] per codeword (k-wide groups), in the
 // K-major no-swizzle layout: codeword n, 16-byte chunk kc of its row at
 // (n / 8) * (KP / 8) * 128 + kc * 128 + (n % 8) * 16, so any run of whole 8-codeword groups (a
-// 128-codeword tile) is contiguous.
+// 256-codeword tile) is contiguous.
 cudaError_t prepare_kq_tc(fq_ctx *ctx) {
     const int N = ctx->N, k = ctx->k, d = ctx->d;
-    const int KP = (3 * k + 2 <= 16) ? 16 : 32;
+    const int KP = (3 * k + 4 <= 16) ? 16 : 32;
     std::vector<float> C((size_t)N * k), P((size_t)d * d);
     cudaError_t e = cudaMemcpy(C.data(), ctx->C, C.size() * 4, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemcpy(P.data(), ctx->Pi, P.size() * 4, cudaMemcpyDeviceToHost);
@@ -586,6 +707,8 @@ cudaError_t prepare_kq_tc(fq_ctx *ctx) {
         split(kOpScale * h, hh, hl);
         row[3 * k] = hh;
         row[3 * k + 1] = hl;
+        row[3 * k + 2] = __float2half_rn(kOpScale);   // times the A row's 2^10 |u_b|^2 halves
+        row[3 * k + 3] = __float2half_rn(kOpScale);
         for (int kc = 0; kc < KP / 8; ++kc)
             for (int q = 0; q < 8; ++q) {
                 const size_t off = (size_t)(n / 8) * (KP / 8) * 64 + (size_t)kc * 64 + (size_t)(n % 8) * 8 + q;
@@ -602,18 +725,19 @@ cudaError_t prepare_kq_tc(fq_ctx *ctx) {
         if (e == cudaSuccess) e = cudaMemcpy(ctx->pi_split, pis.data(), pis.size() * 2, cudaMemcpyHostToDevice);
         if (e != cudaSuccess) return e;
     }
-    if (d == 64 && k == 4) return prep_kq<64, 4, 16>(ctx);
-    if (d == 64 && k == 8) return prep_kq<64, 8, 8>(ctx);
-    if (d == 128 && k == 4) return prep_kq<128, 4, 16>(ctx);
-    return prep_kq<128, 8, 8>(ctx);
+    // Codeword tiles of 256: the widest MMA.
+    if (d == 64 && k == 4) return prep_kq<64, 4, 8, 256>(ctx);
+    if (d == 64 && k == 8) return prep_kq<64, 8, 8, 256>(ctx);
+    if (d == 128 && k == 4) return prep_kq<128, 4, 8, 256>(ctx);
+    return prep_kq<128, 8, 8, 256>(ctx);
 }
 
 cudaError_t launch_encode_kq_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                 uint32_t *codes, cudaStream_t s) {
-    if (ctx->d == 64 && ctx->k == 4) return launch_kq<64, 4, 16>(ctx, x, M, map, nu, codes, s);
-    if (ctx->d == 64 && ctx->k == 8) return launch_kq<64, 8, 8>(ctx, x, M, map, nu, codes, s);
-    if (ctx->d == 128 && ctx->k == 4) return launch_kq<128, 4, 16>(ctx, x, M, map, nu, codes, s);
-    return launch_kq<128, 8, 8>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64 && ctx->k == 4) return launch_kq<64, 4, 8, 256>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 64 && ctx->k == 8) return launch_kq<64, 8, 8, 256>(ctx, x, M, map, nu, codes, s);
+    if (ctx->d == 128 && ctx->k == 4) return launch_kq<128, 4, 8, 256>(ctx, x, M, map, nu, codes, s);
+    return launch_kq<128, 8, 8, 256>(ctx, x, M, map, nu, codes, s);
 }
 
 }  // namespace fq

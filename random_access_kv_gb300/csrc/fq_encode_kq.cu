@@ -559,8 +559,12 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     for (int j = 0; j < OWN; ++j) {
                         const int c0 = cjs[j] * kChunk - base;
                         if (c0 >= 0 && c0 < ncw) {
+                            // Every chunk starts on a 16-codeword boundary, so the lanes read their
+                            // chunks in lane-rotated order (codeword (q + lane) mod 16 at step q) to
+                            // spread the reads over the banks; ties still go to the lowest index.
 #pragma unroll 4
-                            for (int q = 0; q < kChunk; ++q) {
+                            for (int q0 = 0; q0 < kChunk; ++q0) {
+                                const int q = (q0 + lane) & (kChunk - 1);
                                 const float4 *cp = reinterpret_cast<const float4 *>(cs + (size_t)(c0 + q) * K);
                                 float dsum = 0.f;
 #pragma unroll
@@ -573,9 +577,10 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                                     dsum = fmaf(e2, e2, dsum);
                                     dsum = fmaf(e3, e3, dsum);
                                 }
-                                if (dsum < bd[j]) {
+                                const int nq = base + c0 + q;
+                                if (dsum < bd[j] || (dsum == bd[j] && nq < bi[j])) {
                                     bd[j] = dsum;
-                                    bi[j] = base + c0 + q;
+                                    bi[j] = nq;
                                 }
                             }
                         }

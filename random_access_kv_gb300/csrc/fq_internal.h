@@ -29,7 +29,7 @@ struct fq_ctx {
     uint16_t *cb_split;          // [N][2k] fp16 halves of 2^10 c_n (k hi, then k lo)
     uint32_t *cb_lanes;          // d = 64, k <= 2: cb_split's words, each repeated for 32 lanes
     // k = d tensor-core encoder table
-    uint16_t *crot_split;        // [2][N x d] fp16 halves of -2 * 2^12 Crot (hi block, then lo block)
+    uint16_t *crot_split;        // fp16 halves of -2 * 2^12 Crot (hi block [N x d], lo block), then bf16 norm blocks
     // k = 4, 8 tensor-core encoder table
     uint8_t *cb_ops;             // codebook rows as MMA B operands (see fq_encode_kq.cu)
     int kq_max_ctas;

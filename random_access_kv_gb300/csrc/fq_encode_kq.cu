@@ -416,70 +416,46 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     ++n;
                 }
                 // --- score items: this warp's part of the columns of every item --------------------
-                // Loads of 16 columns; the next load is always in flight while the previous 16
-                // columns are folded (tcgen05.wait::ld waits for all loads issued so far, and at each
-                // wait only the newest is outstanding).
+                // All kLd columns of an item in one batch of loads and one wait, then the buffer is
+                // released and the columns are folded.
                 int bkey[NBH], btile[NBH];
 #pragma unroll
                 for (int bb = 0; bb < NBH; ++bb) {
                     bkey[bb] = 0x7FFFFFFF;
                     btile[bb] = 0;
                 }
-                uint32_t rr[2][16];
                 const uint32_t colq = tmem_base + lane_off + (uint32_t)(cq * kLd);
-                // The first item's first 16 columns.
-                {
-                    const uint32_t buf = n & 1u;
-                    ok = __all_sync(0xffffffffu, mbar_wait(ready + buf, (n >> 1) & 1));
-                    if (ok) {
-                        tc_fence_after();
-                        tmem_ld16_nowait(colq + buf * (uint32_t)NT, rr[0]);
-                        tmem_wait_ld();
-                    }
-                }
 #pragma unroll 1
                 for (int bt = 0; bt < nbt && ok; ++bt) {
 #pragma unroll
                     for (int bb = 0; bb < NBH; ++bb) {
                         const uint32_t g = n + (uint32_t)(bt * NBH + bb);
                         const uint32_t buf = g & 1u;
-                        const uint32_t col = colq + buf * (uint32_t)NT;
-                        const bool more = bb + 1 < NBH || bt + 1 < nbt;
+                        ok = __all_sync(0xffffffffu, mbar_wait(ready + buf, (g >> 1) & 1));
+                        if (!ok) break;
+                        tc_fence_after();
+                        uint32_t rr[kLd / 32][32];
+#pragma unroll
+                        for (int h = 0; h < kLd / 32; ++h) tmem_ld32_nowait(colq + buf * (uint32_t)NT + 32 * h, rr[h]);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(freeb + buf);      // the scores are in registers
                         int ikey = 0x7FFFFFFF;
 #pragma unroll
-                        for (int sub = 0; sub < kLd / 16; ++sub) {
-                            const int cur = sub & 1, nxt = cur ^ 1;
-                            if (sub + 1 < kLd / 16) {
-                                tmem_ld16_nowait(col + 16 * (sub + 1), rr[nxt]);
-                            } else if (more) {
-                                // the next item's first 16 columns
-                                const uint32_t gn = g + 1, bn = gn & 1u;
-                                ok = __all_sync(0xffffffffu, mbar_wait(ready + bn, (gn >> 1) & 1));
-                                if (ok) {
-                                    tc_fence_after();
-                                    tmem_ld16_nowait(colq + bn * (uint32_t)NT, rr[nxt]);
-                                }
-                            }
+                        for (int c = 0; c < kLd / kChunk; ++c) {
                             float v[16];
 #pragma unroll
-                            for (int z = 0; z < 16; ++z) v[z] = __uint_as_float(rr[cur][z]);
+                            for (int z = 0; z < 16; ++z) v[z] = __uint_as_float(rr[c / 2][16 * (c % 2) + z]);
 #pragma unroll
                             for (int wd = 8; wd > 0; wd /= 2)
 #pragma unroll
                                 for (int z = 0; z < wd; ++z) v[z] = fminf(v[z], v[z + wd]);
-                            ikey = min(ikey, (int)((__float_as_uint(v[0]) & ~kSubMask) | (uint32_t)sub));
-                            if (sub + 1 < kLd / 16 || more) tmem_wait_ld();
-                            if (sub + 2 == kLd / 16) {
-                                // the item's last load has landed (waited just above): release the buffer
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(freeb + buf);
-                            }
+                            ikey = min(ikey, (int)((__float_as_uint(v[0]) & ~kSubMask) | (uint32_t)c));
                         }
                         const bool better = ikey < bkey[bb];
                         bkey[bb] = better ? ikey : bkey[bb];
                         btile[bb] = better ? bt : btile[bb];
-                        if (!ok) break;
                     }
                 }
                 n += (uint32_t)(nbt * NBH);

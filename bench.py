@@ -112,6 +112,7 @@ def measured_peaks() -> dict:
 # The source file of each timed kernel; its hash (with the shared headers) ties a committed ncu
 # traffic figure to the code it measured.
 KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu"],
+                  "encode_k4_grid": ["fq_encode_k4.cu", "fq_grid4.h"],
                   "encode_full_tc": ["fq_encode_full_tc.cu"], "decode_tc": ["fq_decode_tc.cu"],
                   "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"],
                   "archive_encode": ["fa_archive.cu"], "archive_decode": ["fa_archive.cu"],
@@ -132,7 +133,9 @@ def source_hash(kernel: str) -> str:
 def kernel_of(w, op: str) -> str:
     """Name of the kernel that runs `op` ("encode" or "decode") for workload w."""
     if op == "encode":
-        return "encode_full_tc" if w.k == w.d else ("encode_k2_tc" if w.k == 2 else "encode_kq_tc")
+        if w.k == w.d:
+            return "encode_full_tc"
+        return {2: "encode_k2_tc", 4: "encode_k4_grid"}.get(w.k, "encode_kq_tc")
     return "decode_full" if w.k == w.d else "decode_tc"
 
 

@@ -51,6 +51,10 @@ void free_ctx(fq_ctx *c) {
     cudaFree(c->cb_lanes);
     cudaFree(c->crot_split);
     cudaFree(c->cb_ops);
+    cudaFree(c->k4_cells);
+    cudaFree(c->k4_pool);
+    cudaFree(c->k4_axis);
+    cudaFree(c->k4_ncb);
     free(c);
 }
 
@@ -106,7 +110,8 @@ cudaError_t build_tables(fq_ctx *c, const float *C_host, const float *Pi_host) {
     if (e == cudaSuccess && fq::k2_tc_supported(c)) e = fq::prepare_k2_tc(c);
     if (e == cudaSuccess && !is_full(c) && fq::decode_tc_supported(c)) e = fq::prepare_decode_tc(c);
     if (e == cudaSuccess && is_full(c) && fq::full_tc_supported(c)) e = fq::prepare_full_tc(c);
-    if (e == cudaSuccess && !is_full(c) && !c->grid2 && fq::kq_tc_supported(c)) e = fq::prepare_kq_tc(c);
+    if (e == cudaSuccess && fq::k4_grid_supported(c)) e = fq::prepare_k4_grid(c);
+    if (e == cudaSuccess && !is_full(c) && !c->grid2 && !c->k4_cells && fq::kq_tc_supported(c)) e = fq::prepare_kq_tc(c);
     if (e == cudaSuccess) e = fq::prepare_attend(c);
     return e;
 }
@@ -214,6 +219,8 @@ static int encode_common(fq_ctx *ctx, const void *x, int64_t M, fq::RowMap map, 
         e = fq::launch_encode_full(ctx, (const __half *)x, M, map, nu, codes, s);
     else if (ctx->grid2)
         e = fq::launch_encode_k2_tc(ctx, (const __half *)x, M, map, nu, codes, s);
+    else if (ctx->k4_cells)
+        e = fq::launch_encode_k4_grid(ctx, (const __half *)x, M, map, nu, codes, s);
     else if (ctx->cb_ops)
         e = fq::launch_encode_kq_tc(ctx, (const __half *)x, M, map, nu, codes, s);
     else

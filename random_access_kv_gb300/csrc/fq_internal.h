@@ -30,6 +30,13 @@ struct fq_ctx {
     uint32_t *cb_lanes;          // d = 64, k <= 2: cb_split's words, each repeated for 32 lanes
     // k = d tensor-core encoder table
     uint16_t *crot_split;        // fp16 halves of -2 * 2^12 Crot (hi block [N x d], lo block), then bf16 norm blocks
+    // k = 4 candidate-grid encoder tables
+    uint16_t *k4_cells;          // [G^4][8] cell records (count, up to 7 ascending indices)
+    uint16_t *k4_pool;           // overflow lists of cells with more than 7 candidates
+    uint8_t *k4_axis;            // lattice entry -> coarse cell index per axis (0xFF outside)
+    float *k4_ncb;               // [N x 4] negated codebook
+    float k4_fs;                 // lattice entries per unit of a coordinate
+    int k4_G, k4_max_ctas;
     // k = 4, 8 tensor-core encoder table
     uint8_t *cb_ops;             // codebook rows as MMA B operands (see fq_encode_kq.cu)
     int kq_max_ctas;
@@ -86,6 +93,10 @@ cudaError_t launch_decode_tc(const fq_ctx *ctx, const float *nu, const uint32_t 
 bool full_tc_supported(const fq_ctx *ctx);
 cudaError_t prepare_full_tc(fq_ctx *ctx);
 cudaError_t launch_encode_full_tc(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
+                                  uint32_t *codes, cudaStream_t s);
+bool k4_grid_supported(const fq_ctx *ctx);
+cudaError_t prepare_k4_grid(fq_ctx *ctx);
+cudaError_t launch_encode_k4_grid(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                   uint32_t *codes, cudaStream_t s);
 bool kq_tc_supported(const fq_ctx *ctx);
 cudaError_t prepare_kq_tc(fq_ctx *ctx);

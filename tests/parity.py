@@ -46,8 +46,9 @@ def check_nu(nu_gpu, nu_orc):
     assert not bad.any(), f"nu mismatch at rows {np.flatnonzero(bad)[:5]}: {nu_gpu[bad][:5]} vs {nu_orc[bad][:5]}"
 
 
-def check_indices(x, C, Pi, idx_gpu, rows=None):
-    """Returns (agreement fraction, number of mismatches, max relative gap of mismatches)."""
+def check_indices(x, C, Pi, idx_gpu, rows=None, agreement=AGREEMENT):
+    """Returns (agreement fraction, number of mismatches, max relative gap of mismatches, nu).
+    `agreement` is lowered only for inputs built to sit on near ties."""
     C64 = np.asarray(C, dtype=np.float64)
     k = C64.shape[1]
     nu, idx_orc = ofq.encode(x, C, Pi)
@@ -65,7 +66,7 @@ def check_indices(x, C, Pi, idx_gpu, rows=None):
         worst = max(worst, gap)
         assert gap <= NEAR_TIE_REL, f"row {m} block {b}: index {idx_gpu[m, b]} vs {idx_orc[m, b]}, gap {gap:.3e}"
     agree = 1.0 - len(mism) / max(1, idx_orc.size)
-    assert agree >= AGREEMENT, f"index agreement {agree:.6f} < {AGREEMENT}"
+    assert agree >= agreement, f"index agreement {agree:.6f} < {agreement}"
     return agree, len(mism), worst, nu
 
 

@@ -15,7 +15,8 @@ import bench  # noqa: E402
 
 def test_kernel_names_and_bytes():
     assert bench.kernel_of(synth.WORKLOADS[2], "encode") == "encode_k2_tc"
-    assert bench.kernel_of(synth.WORKLOADS[3], "encode") == "encode_kq_tc"
+    assert bench.kernel_of(synth.WORKLOADS[3], "encode") == "encode_k4_grid"
+    assert bench.kernel_of(synth.WORKLOADS[4], "encode") == "encode_kq_tc"
     assert bench.kernel_of(synth.WORKLOADS[5], "encode") == "encode_full_tc"
     assert bench.kernel_of(synth.WORKLOADS[4], "decode") == "decode_tc"
     enc, gat = bench.workload_bytes(synth.WORKLOADS[2], 256)

@@ -111,7 +111,7 @@ def measured_peaks() -> dict:
 
 # The source file of each timed kernel; its hash (with the shared headers) ties a committed ncu
 # traffic figure to the code it measured.
-KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu"],
+KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu", "fq_tmem_red.cuh"],
                   "encode_k4_grid": ["fq_encode_k4.cu", "fq_grid4.h"],
                   "encode_full_tc": ["fq_encode_full_tc.cu"], "decode_tc": ["fq_decode_tc.cu"],
                   "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"],

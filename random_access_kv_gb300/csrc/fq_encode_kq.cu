@@ -21,19 +21,20 @@
 //   2. Score items: for each NT-codeword tile of the codebook (resident in shared memory when it
 //      fits, else streamed through a ring) and each block of the pass, one MMA into one of two
 //      NT-column TMEM buffers. The two consumer warps of a lane quarter read every item, each
-//      half of the columns (32 rows x 128 scores, in 16-column loads, the next load always in
-//      flight while the previous columns are folded), and release the buffer after their last
-//      load. A 16-column chunk folds to its minimum by a tree of 15 two-input minima (the min
-//      pipe's full rate); the chunk's number within the half goes into the three low mantissa
-//      bits (a relative change below 2^-20 of the score), so one integer minimum per chunk keeps
-//      the running (score, chunk) of the item and the lowest chunk wins a tie. Per (row, block)
-//      the best item so far and its codeword tile are kept (a later tile wins only by a lower key).
+//      half of the columns (32 rows x 128 scores, eight 16-column loads in one batch), and release
+//      the buffer once the loads have landed. Each load is a tcgen05.ld.red: with the columns it
+//      returns their minimum per row, so a 16-column chunk folds to its minimum without CUDA-core
+//      work; the chunk's number within the half goes into the three low mantissa bits (a
+//      relative change below 2^-20 of the score), so one integer minimum per chunk keeps the
+//      running (score, chunk) of the item and the lowest chunk wins a tie. Per (row, block) the
+//      best item so far and its codeword tile are kept (a later tile wins only by a lower key).
 //   3. Resolution: at the end of the pass the two halves' candidates of each (row, block) meet in
 //      shared memory (lower score, then lower codeword index), which gives the 16-codeword chunk
 //      that holds the smallest tensor-core score. Its 16 codewords are scored again on the CUDA
 //      cores by squared difference |u_b - c_n|^2 in fp32 (u_b = (uh + ul) / 2^10, the values the
-//      MMA used), lowest score first, ties to the lowest n. The codeword found is within the
-//      tensor-core scores' rounding (about 2^-20 of the terms) of the true nearest one. The fp32
+//      MMA used; packed two-lane arithmetic), lowest score first, ties to the lowest n. The
+//      codeword found is within the tensor-core scores' rounding (about 2^-20 of the terms) of
+//      the true nearest one. The fp32
 //      codebook is read from shared memory: once u is in registers, the A operands' space takes
 //      it by bulk copies (as many rounds as it needs), so that these random reads never go to L2.
 //   4. Indices are staged in shared memory and packed at the record's fixed bit address; nu is
@@ -47,6 +48,7 @@
 #include "fq_bits.cuh"
 #include "fq_internal.h"
 #include "fq_sm100.cuh"
+#include "fq_tmem_red.cuh"
 
 namespace fq {
 
@@ -434,25 +436,23 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                         ok = __all_sync(0xffffffffu, mbar_wait(ready + buf, (g >> 1) & 1));
                         if (!ok) break;
                         tc_fence_after();
-                        uint32_t rr[kLd / 32][32];
+                        // Each 16-column chunk's minimum comes with its load (tcgen05.ld.red);
+                        // all kLd columns in one batch and one wait, then the buffer is released.
+                        uint32_t rr[kLd / kChunk][16];
+                        float mc[kLd / kChunk];
 #pragma unroll
-                        for (int h = 0; h < kLd / 32; ++h) tmem_ld32_nowait(colq + buf * (uint32_t)NT + 32 * h, rr[h]);
+                        for (int c = 0; c < kLd / kChunk; ++c)
+                            mc[c] = tmem_ldred16_min(colq + buf * (uint32_t)NT + (uint32_t)(kChunk * c), rr[c]);
                         tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < kLd / kChunk; ++c) keep16(rr[c]);
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(freeb + buf);      // the scores are in registers
+                        if (lane == 0) mbar_arrive(freeb + buf);      // the minima are in registers
                         int ikey = 0x7FFFFFFF;
 #pragma unroll
-                        for (int c = 0; c < kLd / kChunk; ++c) {
-                            float v[16];
-#pragma unroll
-                            for (int z = 0; z < 16; ++z) v[z] = __uint_as_float(rr[c / 2][16 * (c % 2) + z]);
-#pragma unroll
-                            for (int wd = 8; wd > 0; wd /= 2)
-#pragma unroll
-                                for (int z = 0; z < wd; ++z) v[z] = fminf(v[z], v[z + wd]);
-                            ikey = min(ikey, (int)((__float_as_uint(v[0]) & ~kSubMask) | (uint32_t)c));
-                        }
+                        for (int c = 0; c < kLd / kChunk; ++c)
+                            ikey = min(ikey, (int)((__float_as_uint(mc[c]) & ~kSubMask) | (uint32_t)c));
                         const bool better = ikey < bkey[bb];
                         bkey[bb] = better ? ikey : bkey[bb];
                         btile[bb] = better ? bt : btile[bb];
@@ -515,10 +515,13 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                 named_sync(1, kCons);
                 float bd[OWN];
                 int bi[OWN];
+                float2 nu2[OWN][K / 2];            // -u in pairs, for the packed differences
 #pragma unroll
                 for (int j = 0; j < OWN; ++j) {
                     bd[j] = INFINITY;
                     bi[j] = cjs[j] * kChunk;
+#pragma unroll
+                    for (int e = 0; e < K / 2; ++e) nu2[j][e] = make_float2(-u[j][2 * e], -u[j][2 * e + 1]);
                 }
                 const float *cs = reinterpret_cast<const float *>(sm + L::oA);
 #pragma unroll 1
@@ -542,17 +545,18 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                             for (int q0 = 0; q0 < kChunk; ++q0) {
                                 const int q = (q0 + lane) & (kChunk - 1);
                                 const float4 *cp = reinterpret_cast<const float4 *>(cs + (size_t)(c0 + q) * K);
-                                float dsum = 0.f;
+                                // |c - u|^2 in packed fp32 pairs: e = c + (-u), then the squares
+                                // summed pairwise and the two lanes added.
+                                float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                                 for (int e = 0; e < K / 4; ++e) {
                                     const float4 c = cp[e];
-                                    const float e0 = u[j][4 * e] - c.x, e1 = u[j][4 * e + 1] - c.y;
-                                    const float e2 = u[j][4 * e + 2] - c.z, e3 = u[j][4 * e + 3] - c.w;
-                                    dsum = fmaf(e0, e0, dsum);
-                                    dsum = fmaf(e1, e1, dsum);
-                                    dsum = fmaf(e2, e2, dsum);
-                                    dsum = fmaf(e3, e3, dsum);
+                                    const float2 e01 = __fadd2_rn(make_float2(c.x, c.y), nu2[j][2 * e]);
+                                    const float2 e23 = __fadd2_rn(make_float2(c.z, c.w), nu2[j][2 * e + 1]);
+                                    acc = __ffma2_rn(e01, e01, acc);
+                                    acc = __ffma2_rn(e23, e23, acc);
                                 }
+                                const float dsum = acc.x + acc.y;
                                 const int nq = base + c0 + q;
                                 if (dsum < bd[j] || (dsum == bd[j] && nq < bi[j])) {
                                     bd[j] = dsum;

@@ -21,16 +21,16 @@
 //   2. Score items: for each NT-codeword tile of the codebook (resident in shared memory when it
 //      fits, else streamed through a ring) and each block of the pass, one MMA into one of two
 //      NT-column TMEM buffers. The two consumer warps of a lane quarter read every item, each
-//      half of the columns (32 rows x 128 scores, eight 16-column loads in one batch), and release
+//      half of the columns (32 rows x 128 scores, sixteen 8-column loads in one batch), and release
 //      the buffer once the loads have landed. Each load is a tcgen05.ld.red: with the columns it
-//      returns their minimum per row, so a 16-column chunk folds to its minimum without CUDA-core
-//      work; the chunk's number within the half goes into the three low mantissa bits (a
-//      relative change below 2^-20 of the score), so one integer minimum per chunk keeps the
+//      returns their minimum per row, so an 8-column chunk folds to its minimum without CUDA-core
+//      work; the chunk's number within the half goes into the four low mantissa bits (a
+//      relative change below 2^-19 of the score), so one integer minimum per chunk keeps the
 //      running (score, chunk) of the item and the lowest chunk wins a tie. Per (row, block) the
 //      best item so far and its codeword tile are kept (a later tile wins only by a lower key).
 //   3. Resolution: at the end of the pass the two halves' candidates of each (row, block) meet in
-//      shared memory (lower score, then lower codeword index), which gives the 16-codeword chunk
-//      that holds the smallest tensor-core score. Its 16 codewords are scored again on the CUDA
+//      shared memory (lower score, then lower codeword index), which gives the 8-codeword chunk
+//      that holds the smallest tensor-core score. Its 8 codewords are scored again on the CUDA
 //      cores by squared difference |u_b - c_n|^2 in fp32 (u_b = (uh + ul) / 2^10, the values the
 //      MMA used; packed two-lane arithmetic), lowest score first, ties to the lowest n. The
 //      codeword found is within the tensor-core scores' rounding (about 2^-20 of the terms) of
@@ -57,7 +57,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kRows = 128;
-constexpr int kChunk = 16;                // codewords per tracked chunk
+constexpr int kChunk = 8;                 // codewords per tracked chunk
 constexpr int kBufs = 2;                  // TMEM score buffers of NT columns
 constexpr int kQ = 2;                     // consumer warps per TMEM lane quarter (column parts of an item)
 constexpr int kConsumerWarps = 4 * kQ;
@@ -436,16 +436,16 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                         ok = __all_sync(0xffffffffu, mbar_wait(ready + buf, (g >> 1) & 1));
                         if (!ok) break;
                         tc_fence_after();
-                        // Each 16-column chunk's minimum comes with its load (tcgen05.ld.red);
+                        // Each 8-column chunk's minimum comes with its load (tcgen05.ld.red);
                         // all kLd columns in one batch and one wait, then the buffer is released.
-                        uint32_t rr[kLd / kChunk][16];
+                        uint32_t rr[kLd / kChunk][8];
                         float mc[kLd / kChunk];
 #pragma unroll
                         for (int c = 0; c < kLd / kChunk; ++c)
-                            mc[c] = tmem_ldred16_min(colq + buf * (uint32_t)NT + (uint32_t)(kChunk * c), rr[c]);
+                            mc[c] = tmem_ldred8_min(colq + buf * (uint32_t)NT + (uint32_t)(kChunk * c), rr[c]);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < kLd / kChunk; ++c) keep16(rr[c]);
+                        for (int c = 0; c < kLd / kChunk; ++c) keep8(rr[c]);
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(freeb + buf);      // the minima are in registers

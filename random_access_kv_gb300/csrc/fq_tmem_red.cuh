@@ -27,6 +27,21 @@ __device__ __forceinline__ float tmem_ldred16_min(uint32_t taddr, uint32_t (&v)[
     return m;
 }
 
+// Minimum over 8 consecutive fp32 columns (as tmem_ldred16_min).
+__device__ __forceinline__ float tmem_ldred8_min(uint32_t taddr, uint32_t (&v)[8]) {
+    float m;
+    asm volatile("tcgen05.ld.red.sync.aligned.32x32b.x8.min.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, %8, [%9];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                   "=f"(m)
+                 : "r"(taddr)
+                 : "memory");
+    return m;
+}
+
+__device__ __forceinline__ void keep8(const uint32_t (&v)[8]) {
+    asm volatile("" ::"r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]));
+}
+
 // Marks 16 registers as read here (no instruction): keeps a load's destination registers
 // reserved until after tcgen05.wait::ld.
 __device__ __forceinline__ void keep16(const uint32_t (&v)[16]) {

@@ -99,7 +99,7 @@ struct KQ {
     static_assert(kBars * 8 <= 512, "barrier space");
     static_assert(kPassCols % 32 == 0 && kPassCols <= 64, "one pass reads 32 or 64 columns of Y");
     static_assert(kBufs * NT <= 512, "tensor memory");
-    static_assert(kLd % 32 == 0 && kPassCols <= NT, "score buffers: 16-column loads, an even number per consumer warp and item");
+    static_assert(kLd % 32 == 0 && kPassCols <= NT, "score buffers: whole 32-column groups per consumer warp and item");
     static_assert(kResCw % kChunk == 0, "resolution rounds hold whole chunks");
     static_assert(NBH % kQ == 0, "the consumer warps of a lane quarter split the blocks' A rows");
 };
@@ -538,9 +538,10 @@ encode_kq_tc(const __grid_constant__ CUtensorMap xmap, const KQParams p) {
                     for (int j = 0; j < OWN; ++j) {
                         const int c0 = cjs[j] * kChunk - base;
                         if (c0 >= 0 && c0 < ncw) {
-                            // Every chunk starts on a 16-codeword boundary, so the lanes read their
-                            // chunks in lane-rotated order (codeword (q + lane) mod 16 at step q) to
-                            // spread the reads over the banks; ties still go to the lowest index.
+                            // Every chunk starts on a kChunk-codeword boundary, so the lanes read
+                            // their chunks in lane-rotated order (codeword (q + lane) mod kChunk at
+                            // step q) to spread the reads over the banks; ties still go to the
+                            // lowest index.
 #pragma unroll 4
                             for (int q0 = 0; q0 < kChunk; ++q0) {
                                 const int q = (q0 + lane) & (kChunk - 1);

@@ -113,7 +113,7 @@ def measured_peaks() -> dict:
 # traffic figure to the code it measured.
 KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu", "fq_tmem_red.cuh"],
                   "encode_k4_grid": ["fq_encode_k4.cu", "fq_grid4.h"],
-                  "encode_full_tc": ["fq_encode_full_tc.cu"], "decode_tc": ["fq_decode_tc.cu"],
+                  "encode_full_tc": ["fq_encode_full_tc.cu", "fq_tmem_red.cuh"], "decode_tc": ["fq_decode_tc.cu"],
                   "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"],
                   "archive_encode": ["fa_archive.cu"], "archive_decode": ["fa_archive.cu"],
                   "archive_access": ["fa_archive.cu"]}

@@ -14,11 +14,14 @@
 // Persistent CTAs of 4 row groups x 128 rows share every codebook tile, streamed through a shared-
 // memory ring by a loader warp. Two MMA warps issue (each for two row groups, descriptors built once);
 // one TMEM buffer of 128 columns per group. 8 consumer warps (two per lane quarter, each serving two
-// groups) read each score item, release the buffer and fold it branch-free: the scores are
-// non-negative distances (up to rounding), so their bits order like integers; each score takes its
-// column within a 16-column chunk in its 4 low mantissa bits (a relative change below 2^-19), a tree
-// of 15 integer minima gives the chunk's (score, column), and one compare and two selects keep the
-// row's best (chunk, key). Ties go to the lowest column, then to the earliest chunk: the lowest n.
+// groups) read each score item with tcgen05.ld.red (each 16-column chunk's minimum comes with the
+// load), release the buffer, and fold: the scores are non-negative distances (up to rounding), so
+// their bits order like integers; each score takes its column within its chunk in its 4 low
+// mantissa bits (a relative change below 2^-19), a tree of 15 integer minima gives the chunk's
+// (score, column), and one compare and two selects keep the row's best (chunk, key). Ties go to the
+// lowest column, then to the earliest chunk: the lowest n. A chunk whose minimum is above every
+// lane's best (by the same key order) cannot change any row's best and is skipped whole; after the
+// first codebook tiles most chunks are.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -29,6 +32,7 @@
 #include "fq_bits.cuh"
 #include "fq_internal.h"
 #include "fq_sm100.cuh"
+#include "fq_tmem_red.cuh"
 
 namespace fq {
 
@@ -271,19 +275,26 @@ encode_full_tc(const __grid_constant__ CUtensorMap xmap, const __grid_constant__
                         break;
                     }
                     tc_fence_after();
-                    uint32_t sc[kNT / 32][32];
+                    // Each 16-column chunk with its minimum (tcgen05.ld.red), one batch, one wait.
+                    uint32_t sc[kNT / kChunk][16];
+                    float mc[kNT / kChunk];
                     const uint32_t col = tmem_base + lane_off + (uint32_t)(g * kNT);
 #pragma unroll
-                    for (int c = 0; c < kNT / 32; ++c) tmem_ld32_nowait(col + 32 * c, sc[c]);
+                    for (int c = 0; c < kNT / kChunk; ++c) mc[c] = tmem_ldred16_min(col + kChunk * c, sc[c]);
                     tmem_wait_ld();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(freeb + g);            // the scores are in registers
 #pragma unroll
                     for (int c = 0; c < kNT / kChunk; ++c) {
+                        // A chunk can change a row's best only if its minimum's key is not above
+                        // the best key (or the minimum is negative, where float and key order
+                        // differ): chunks that no lane of the warp needs are skipped.
+                        const bool may = (int)(__float_as_uint(mc[c]) & ~15u) <= (bkey[gg] & ~15) || mc[c] < 0.f;
+                        if (!__any_sync(0xffffffffu, may)) continue;
                         int v[16];
 #pragma unroll
-                        for (int z = 0; z < 16; ++z) v[z] = (int)((sc[c / 2][16 * (c % 2) + z] & ~15u) | (uint32_t)z);
+                        for (int z = 0; z < 16; ++z) v[z] = (int)((sc[c][z] & ~15u) | (uint32_t)z);
 #pragma unroll
                         for (int wd = 8; wd > 0; wd /= 2)
 #pragma unroll

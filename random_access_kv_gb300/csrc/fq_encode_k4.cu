@@ -11,13 +11,16 @@
 //      u = Y / (2^12 nu). Each block's four coordinates pick a cell of a G^4 candidate grid
 //      (a lattice index per coordinate, one fused multiply-add rounded to an integer, mapped to
 //      a coarse index by a table that every lane reads from its own copy, without bank conflicts).
-//      The cell's 16-byte record, read through the read-only cache from a table that stays in
+//      The cell's 32-byte record, read through the read-only cache from a table that stays in
 //      L2, lists every codeword that can be nearest to some point of the cell (built on the host
 //      from exact box bounds, see fq_grid4.h). The listed codewords are compared by squared
 //      difference |u_b - c|^2 in fp32 (packed two-lane arithmetic), in ascending index order,
 //      ties to the lowest index. Blocks outside the grid, or in a cell that lists more than
-//      seven codewords, are redone afterwards: over the cell's overflow list or the whole
+//      fifteen codewords, are redone afterwards: over the cell's overflow list or the whole
 //      codebook.
+// At d = 64 a CTA runs five row groups with one x tile each: more warps hide more of the record
+// loads' latency, and a second tile per group would leave the record loads, which pass through
+// L1, too little of it (measured slower).
 //   5. Indices are packed LSB-first at the record's fixed bit address; nu is stored.
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -499,15 +502,14 @@ cudaError_t prepare_k4_grid(fq_ctx *ctx) {
     if (e == cudaSuccess) e = upload_vec(&ctx->k4_axis, grid.axis);
     if (e == cudaSuccess) e = upload_vec(&ctx->k4_ncb, ncb);
     if (e != cudaSuccess) return e;
-    if (d == 64) return N <= 2048 ? prep_k4<64, 4, 2>(ctx) : prep_k4<64, 4, 1>(ctx);
+    if (d == 64) return prep_k4<64, 5, 1>(ctx);
     return prep_k4<128, 2, 1>(ctx);
 }
 
 cudaError_t launch_encode_k4_grid(const fq_ctx *ctx, const __half *x, int64_t M, RowMap map, float *nu,
                                   uint32_t *codes, cudaStream_t s) {
     if (ctx->d == 64)
-        return ctx->N <= 2048 ? launch_k4<64, 4, 2>(ctx, x, M, map, nu, codes, s)
-                              : launch_k4<64, 4, 1>(ctx, x, M, map, nu, codes, s);
+        return launch_k4<64, 5, 1>(ctx, x, M, map, nu, codes, s);
     return launch_k4<128, 2, 1>(ctx, x, M, map, nu, codes, s);
 }
 

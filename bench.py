@@ -114,6 +114,7 @@ def measured_peaks() -> dict:
 KERNEL_SOURCES = {"encode_k2_tc": ["fq_encode_k2.cu"], "encode_kq_tc": ["fq_encode_kq.cu", "fq_tmem_red.cuh"],
                   "encode_k4_grid": ["fq_encode_k4.cu", "fq_grid4.h"],
                   "encode_full_tc": ["fq_encode_full_tc.cu", "fq_tmem_red.cuh"], "decode_tc": ["fq_decode_tc.cu"],
+                  "decode_ws": ["fq_decode_tc.cu"],
                   "decode_full": ["fq_full.cu"], "attend": ["fq_attend_kernel.cuh"],
                   "archive_encode": ["fa_archive.cu"], "archive_decode": ["fa_archive.cu"],
                   "archive_access": ["fa_archive.cu"]}
@@ -136,7 +137,9 @@ def kernel_of(w, op: str) -> str:
         if w.k == w.d:
             return "encode_full_tc"
         return {2: "encode_k2_tc", 4: "encode_k4_grid"}.get(w.k, "encode_kq_tc")
-    return "decode_full" if w.k == w.d else "decode_tc"
+    if w.k == w.d:
+        return "decode_full"
+    return "decode_ws" if w.d == 128 else "decode_tc"
 
 
 def committed_traffic(kernel: str, workload, rows_per_launch: int):

@@ -137,7 +137,7 @@ struct RowData {
     uint32_t w[W > 0 ? W : 1];
 };
 
-template <int D, int K, int BS>
+template <int D, int K, int BS, bool NU = true>
 __device__ __forceinline__ RowData<(BS ? (D / K) * BS / 32 : 0)> load_row(const DecParams &p, int64_t tile, int t) {
     constexpr int W = BS ? (D / K) * BS / 32 : 0;
     RowData<W> r;
@@ -145,7 +145,7 @@ __device__ __forceinline__ RowData<(BS ? (D / K) * BS / 32 : 0)> load_row(const 
     r.live = r.j < p.n;
     r.row = r.live ? (p.idx ? __ldg(p.idx + r.j) : r.j) : 0;
     r.valid = r.live && r.row >= 0 && r.row < p.M;
-    r.s = r.valid ? __ldg(p.nu + r.row) * kOutScale : 0.f;
+    r.s = (NU && r.valid) ? __ldg(p.nu + r.row) * kOutScale : 0.f;
     if constexpr (W > 0) {
         const uint32_t *src = p.codes + (r.valid ? r.row : 0) * W;
         if constexpr (W % 4 == 0) {
@@ -172,6 +172,62 @@ __device__ __forceinline__ uint32_t field(const uint32_t (&w)[W], int b) {
     if (o + BS <= 32 || q + 1 >= W) v = w[q] >> o;
     else v = __funnelshift_r(w[q], w[q + 1], o);
     return v & ((1u << BS) - 1u);
+}
+
+// Row t of the two A operands (fp16 halves of 2^10 y_hat, 128-byte swizzle) from the row's
+// record, one 16-byte chunk (8 columns) at a time: the d/k codewords of the record, concatenated.
+// A row that is not valid is written as zeros.
+template <int D, int K, int CBM, int BS, int W>
+__device__ __forceinline__ void build_a_row(const DecParams &p, const RowData<W> &cur, const uint16_t *cb,
+                                            uint8_t *a_hi, uint8_t *a_lo, int t) {
+    const int R = (D / K) * p.B;
+    BitReader rd(p.codes, (BS == 0 && cur.valid) ? cur.row * (int64_t)R : 0, BS == 0 && cur.valid);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+        uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+        if (cur.valid) {
+            constexpr int BPC = K >= 2 ? 8 / K : 8;      // blocks per chunk
+#pragma unroll
+            for (int b = 0; b < BPC; ++b) {
+                uint32_t i;
+                if constexpr (BS != 0) i = field<BS, W>(cur.w, c * BPC + b);
+                else i = rd.get(p.B);
+                const CwHalves<K> v = fetch_cw<K, CBM>(cb, i, t & 31);
+                if constexpr (K >= 2) {
+#pragma unroll
+                    for (int q = 0; q < K / 2; ++q) {
+                        hw[b * (K / 2) + q] = v.hi[q];
+                        lw[b * (K / 2) + q] = v.lo[q];
+                    }
+                } else {
+                    hw[b / 2] |= v.hi[0] << (16 * (b & 1));
+                    lw[b / 2] |= v.lo[0] << (16 * (b & 1));
+                }
+            }
+        }
+        const int kb = c / 8, cc = c % 8;
+        const uint32_t off = (uint32_t)(kb * 16384 + t * 128 + ((cc ^ (t & 7)) << 4));
+        *reinterpret_cast<uint4 *>(a_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4 *>(a_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+}
+
+// Y_hat Pi^T-split into a 128 x D fp32 accumulator: hi*Pi_hi + hi*Pi_lo + lo*Pi_hi, D/16
+// K-steps each (A: 128 rows x D fp16 in 64-column swizzled blocks of 16 KB; B likewise, D rows).
+template <int D>
+__device__ __forceinline__ void issue_rotation(uint32_t acc, uint32_t ah, uint32_t al, uint32_t pb_hi, uint32_t pb_lo) {
+    const uint32_t idesc = idesc_f16_f32(128, D);
+#pragma unroll
+    for (int pass = 0; pass < 3; ++pass) {
+        const uint32_t aa = pass == 2 ? al : ah;
+        const uint32_t bb = pass == 1 ? pb_lo : pb_hi;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t aoff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
+            const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
+            mma_f16(acc, sdesc_sw128(aa + aoff), sdesc_sw128(bb + boff), idesc, (pass | kk) ? 1u : 0u);
+        }
+    }
 }
 
 template <int D, int K, int NG, int CBM, int BS, typename OutT>
@@ -225,9 +281,6 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const __grid_constant__
     RowData<W> cur = load_row<D, K, BS>(p, first, t);
     bool ok = named_sync_and(1 + g, 128, mbar_wait(bar_tab, 0));
 
-    constexpr int NB = D / K;
-    const int R = NB * p.B;
-    const uint32_t idesc = idesc_f16_f32(128, D);
     const uint32_t tmem_acc = tmem_base + (uint32_t)(g * D);
     const uint32_t pb_hi = smem_addr(sm + L::oPi), pb_lo = pb_hi + L::kPiPart;
     OutT *out = reinterpret_cast<OutT *>(p.out);
@@ -237,52 +290,12 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const __grid_constant__
         // Requests for the next tile go out now and land while this one is processed.
         const RowData<W> nxt = load_row<D, K, BS>(p, tile + gstride, t);
         if (cur.live && !cur.valid) atomicOr(p.flags, (uint32_t)FQ_FLAG_RANGE);
-        BitReader rd(p.codes, (BS == 0 && cur.valid) ? cur.row * (int64_t)R : 0, BS == 0 && cur.valid);
-        // Row t of the two A operands, one 16-byte chunk (8 columns) at a time.
-#pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-            if (cur.valid) {
-                constexpr int BPC = K >= 2 ? 8 / K : 8;      // blocks per chunk
-#pragma unroll
-                for (int b = 0; b < BPC; ++b) {
-                    uint32_t i;
-                    if constexpr (BS != 0) i = field<BS, W>(cur.w, c * BPC + b);
-                    else i = rd.get(p.B);
-                    const CwHalves<K> v = fetch_cw<K, CBM>(cb, i, t & 31);
-                    if constexpr (K >= 2) {
-#pragma unroll
-                        for (int q = 0; q < K / 2; ++q) {
-                            hw[b * (K / 2) + q] = v.hi[q];
-                            lw[b * (K / 2) + q] = v.lo[q];
-                        }
-                    } else {
-                        hw[b / 2] |= v.hi[0] << (16 * (b & 1));
-                        lw[b / 2] |= v.lo[0] << (16 * (b & 1));
-                    }
-                }
-            }
-            const int kb = c / 8, cc = c % 8;
-            const uint32_t off = (uint32_t)(kb * 16384 + t * 128 + ((cc ^ (t & 7)) << 4));
-            *reinterpret_cast<uint4 *>(a_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(a_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
+        build_a_row<D, K, CBM, BS, W>(p, cur, cb, a_hi, a_lo, t);
         fence_proxy_async_smem();
         named_sync(1 + g, 128);
         if (t == 0) {
             tc_fence_after();
-            const uint32_t ah = smem_addr(a_hi), al = smem_addr(a_lo);
-#pragma unroll
-            for (int pass = 0; pass < 3; ++pass) {
-                const uint32_t aa = pass == 2 ? al : ah;
-                const uint32_t bb = pass == 1 ? pb_lo : pb_hi;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t aoff = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-                    const uint32_t boff = (uint32_t)((kk >> 2) * (D * 128) + (kk & 3) * 32);
-                    mma_f16(tmem_acc, sdesc_sw128(aa + aoff), sdesc_sw128(bb + boff), idesc, (pass | kk) ? 1u : 0u);
-                }
-            }
+            issue_rotation<D>(tmem_acc, smem_addr(a_hi), smem_addr(a_lo), pb_hi, pb_lo);
             mma_commit(bar_mma);
         }
         ok = named_sync_and(1 + g, 128, mbar_wait(bar_mma, (uint32_t)(it & 1)));
@@ -339,6 +352,284 @@ __global__ void __launch_bounds__(NG * 128, 1) decode_tc(const __grid_constant__
     if (tid < 32) tmem_dealloc(tmem_base, L::kTmemCols);
 }
 
+// ---- d = 128: warp-specialised pipeline -----------------------------------------------------
+//
+// At d = 128 one A operand pair (hi, lo) is 64 KB and the rotation another 64 KB, so only two
+// row groups fit and each ran its phases (A rows, MMAs, read-back and store) one after another.
+// Here the phases of consecutive tiles overlap instead, through two A buffers, two TMEM
+// accumulators and one output stage (224 KB of shared memory):
+//   warps 0-7   two builder groups of 128 threads; group b writes the A rows of the CTA's tiles
+//               i = b, b + 2, ... into A buffer b (one thread per row; at k = 8 one 256-bit load
+//               per codeword), then arrives on a_full[b];
+//   warp 16     one thread issues each tile's three MMAs into accumulator i % 2 once its A rows are
+//               written and the accumulator is free, and commits to mma_done[i % 2] (which also
+//               frees A buffer i % 2 for the builders);
+//   warps 8-15  the read-back: warp 8 + 4h + q reads TMEM lanes 32q .. 32q + 31 (its rows),
+//               columns 64h .. 64h + 63, releases the accumulator (acc_empty), scales by nu, and
+//               stages fp16 rows for one TMA tensor store per 64-column box (fp32 rows are stored
+//               directly). These threads read the row's index and nu themselves, ahead of use.
+// The source rows, records and norms of later tiles are requested early enough that no step
+// waits on a load issued in the same iteration.
+// Every wait is bounded; a wait that gives up sets FQ_FLAG_TIMEOUT and its role stops.
+struct WsLayout {
+    static constexpr int D = 128;
+    static constexpr int kPiPart = D * D * 2;                    // 32 KB
+    static constexpr int kATile = kTileRows * D * 2;             // 32 KB: one fp16 operand
+    static constexpr int oPi = 0;
+    static constexpr int oA = oPi + 2 * kPiPart;                 // two (hi, lo) buffers
+    static constexpr int oOut = oA + 2 * 2 * kATile;             // the fp16 output stage
+    static constexpr int oBar = oOut + kATile;
+    static constexpr int kBars = 7;                              // tables, a_full[2], mma_done[2], acc_empty[2]
+    static constexpr int oTmem = oBar + kBars * 8;
+    static constexpr int kBytes = oTmem + 16 + 1024;
+    static constexpr uint32_t kTmemCols = 2 * D;
+};
+constexpr int kWsEpiWarp = 8, kWsMmaWarp = 16, kWsThreads = 17 * 32, kWsEpiThreads = 256;
+
+// The source row of output row j: its gather index, or j itself. Rows past n read the last index
+// (a valid address); whether a row is live and valid is decided where the value is used, so that
+// nothing waits on the load in the iteration that issues it.
+__device__ __forceinline__ int64_t src_row(const DecParams &p, int64_t j) {
+    return p.idx ? __ldg(p.idx + (j < p.n ? j : p.n - 1)) : j;
+}
+
+__device__ __forceinline__ bool row_valid(const DecParams &p, int64_t j, int64_t row) {
+    return j < p.n && row >= 0 && row < p.M;
+}
+
+// A record held in registers (W words; none when fields are read at run time).
+template <int W>
+struct Rec {
+    uint32_t w[W > 0 ? W : 1];
+};
+
+template <int W>
+__device__ __forceinline__ Rec<W> load_rec(const DecParams &p, int64_t row, bool valid) {
+    Rec<W> r;
+#pragma unroll
+    for (int q = 0; q < (W > 0 ? W : 1); ++q) r.w[q] = 0u;
+    if constexpr (W > 0) {
+        const uint32_t *src = p.codes + (valid ? row : 0) * W;
+#pragma unroll
+        for (int q = 0; q < W; ++q) r.w[q] = valid ? __ldg(src + q) : 0u;
+    }
+    return r;
+}
+
+// 32 bytes (one sector) from read-only global memory in one 256-bit load, not kept in L1.
+// The address must be 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const void *src, uint32_t (&r)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(src));
+}
+
+// k = 8 A rows: each codeword's 32 bytes (fp16 hi half, then lo half) are one sector, read by one
+// 256-bit load and written as one 16-byte chunk of each A operand. Eight codewords are in flight
+// at a time. A row that is not valid is written as zeros.
+template <int BS, int W>
+__device__ __forceinline__ void build_k8_row(const DecParams &p, int64_t row, bool valid, const Rec<W> &rec,
+                                             uint8_t *a_hi, uint8_t *a_lo, int t) {
+    constexpr int D = 128, K = 8;
+    BitReader rd(p.codes, (BS == 0 && valid) ? row * (int64_t)((D / K) * p.B) : 0, BS == 0 && valid);
+#pragma unroll
+    for (int c0 = 0; c0 < D / 8; c0 += 8) {
+        uint32_t v[8][8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) v[c][m] = 0u;
+            if (valid) {
+                uint32_t i;
+                if constexpr (BS != 0) i = field<BS, W>(rec.w, c0 + c);
+                else i = rd.get(p.B);
+                ld_nc_v8(p.cb + (size_t)i * 2 * K, v[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int ch = c0 + c, kb = ch / 8, cc = ch % 8;
+            const uint32_t off = (uint32_t)(kb * 16384 + t * 128 + ((cc ^ (t & 7)) << 4));
+            *reinterpret_cast<uint4 *>(a_hi + off) = make_uint4(v[c][0], v[c][1], v[c][2], v[c][3]);
+            *reinterpret_cast<uint4 *>(a_lo + off) = make_uint4(v[c][4], v[c][5], v[c][6], v[c][7]);
+        }
+    }
+}
+
+template <int K, int BS, typename OutT>
+__global__ void __launch_bounds__(kWsThreads, 1) decode_ws(const __grid_constant__ CUtensorMap omap, const DecParams p) {
+    constexpr int D = 128;
+    constexpr bool TMA_OUT = sizeof(OutT) == 2;
+    constexpr int W = BS ? (D / K) * BS / 32 : 0;
+    using L = WsLayout;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *sm = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
+    uint64_t *bar_tab = bars, *a_full = bars + 1, *mma_done = bars + 3, *acc_empty = bars + 5;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oTmem);
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int64_t ntiles = (p.n + kTileRows - 1) / kTileRows;
+    const int64_t first = blockIdx.x, gstride = gridDim.x;
+
+    if (tid == 0) {
+        mbar_init(bar_tab, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(a_full + b, 1);
+            mbar_init(mma_done + b, 1);
+            mbar_init(acc_empty + b, 8);                 // one arrival per read-back warp
+        }
+        fence_barrier_init();
+    }
+    if (warp == kWsMmaWarp) tmem_alloc(tmem_slot, L::kTmemCols);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(bar_tab, 2u * L::kPiPart);
+        bulk_g2s(sm + L::oPi, p.pit_split, 2u * L::kPiPart, bar_tab);
+        if (TMA_OUT) prefetch_tensormap(&omap);
+    }
+    // Indices, norms and codes may be written by the previous kernel in the stream.
+    griddep_launch_dependents();
+    griddep_wait();
+
+    bool ok = true;
+    if (warp < kWsEpiWarp) {
+        // Builder thread t of group b writes row t of the group's tiles. Source rows are read two
+        // of the group's tiles ahead and records one ahead.
+        const int b = warp / 4, t = tid % 128;
+        uint8_t *a_hi = sm + L::oA + b * 2 * L::kATile;
+        uint8_t *a_lo = a_hi + L::kATile;
+        auto jrow = [&](int64_t i) { return (first + i * gstride) * kTileRows + t; };
+        int64_t row_c = src_row(p, jrow(b)), row_n = src_row(p, jrow(b + 2));
+        Rec<W> rec_c = load_rec<W>(p, row_c, row_valid(p, jrow(b), row_c));
+        for (int64_t i = b; first + i * gstride < ntiles; i += 2) {
+            const Rec<W> rec_n = load_rec<W>(p, row_n, row_valid(p, jrow(i + 2), row_n));
+            const int64_t row_nn = src_row(p, jrow(i + 4));
+            const bool valid = row_valid(p, jrow(i), row_c);
+            if (jrow(i) < p.n && !valid) atomicOr(p.flags, (uint32_t)FQ_FLAG_RANGE);
+            if (i >= 2) {
+                // The MMAs of tile i - 2 have read this buffer.
+                ok = named_sync_and(1 + b, 128, mbar_wait(mma_done + b, (uint32_t)(((i >> 1) - 1) & 1)));
+                if (!ok) break;
+            }
+            if constexpr (K == 8) {
+                build_k8_row<BS, W>(p, row_c, valid, rec_c, a_hi, a_lo, t);
+            } else {
+                RowData<W> rd;
+                rd.j = jrow(i);
+                rd.row = row_c;
+                rd.live = rd.j < p.n;
+                rd.valid = valid;
+                rd.s = 0.f;
+#pragma unroll
+                for (int q = 0; q < (W > 0 ? W : 1); ++q) rd.w[q] = rec_c.w[q];
+                build_a_row<D, K, kCbGlobal, BS, W>(p, rd, p.cb, a_hi, a_lo, t);
+            }
+            fence_proxy_async_smem();
+            named_sync(1 + b, 128);
+            if (t == 0) mbar_arrive(a_full + b);
+            rec_c = rec_n;
+            row_c = row_n;
+            row_n = row_nn;
+        }
+    } else if (warp < kWsMmaWarp) {
+        // Read-back warp 8 + 4h + q: rows 32q .. 32q + 31 (TMEM lanes), columns 64h .. 64h + 63.
+        const int et = tid - kWsEpiWarp * 32, wq = warp % 4, h = (warp - kWsEpiWarp) / 4;
+        const int e = 32 * wq + lane;                    // the row
+        uint8_t *stage = sm + L::oOut;
+        OutT *out = reinterpret_cast<OutT *>(p.out);
+        // Source rows two tiles ahead, nu one tile ahead; the scale is formed where it is used.
+        auto jrow = [&](int64_t i) { return (first + i * gstride) * kTileRows + e; };
+        int64_t row_n = src_row(p, jrow(1));
+        const int64_t row0 = src_row(p, jrow(0));
+        float nu_c = row_valid(p, jrow(0), row0) ? __ldg(p.nu + row0) : 0.f;
+        for (int64_t i = 0; first + i * gstride < ntiles; ++i) {
+            const int b = (int)(i & 1);
+            const int64_t tile = first + i * gstride;
+            const float nu_n = row_valid(p, jrow(i + 1), row_n) ? __ldg(p.nu + row_n) : 0.f;
+            const int64_t row_nn = src_row(p, jrow(i + 2));
+            const float sc = nu_c * kOutScale;
+            const int64_t jc = jrow(i);
+            const bool w = mbar_wait(mma_done + b, (uint32_t)((i >> 1) & 1));
+            if (TMA_OUT && et == 0) bulk_wait_read0();   // the previous tile's store has read the stage
+            ok = named_sync_and(3, kWsEpiThreads, w);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t acc = tmem_base + (uint32_t)(b * D + 64 * h) + ((uint32_t)(32 * wq) << 16);
+            uint32_t r[4][16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld16_nowait(acc + (uint32_t)(16 * q), r[q]);
+            tmem_wait_ld();
+            // This warp's reads of the accumulator are done.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + b);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float v[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) v[m] = __uint_as_float(r[q][m]);
+                if constexpr (TMA_OUT) {
+                    uint32_t hw[8];
+#pragma unroll
+                    for (int m = 0; m < 8; ++m) {
+                        const __half2 hv = __floats2half2_rn(v[2 * m] * sc, v[2 * m + 1] * sc);
+                        hw[m] = *reinterpret_cast<const uint32_t *>(&hv);
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cc = 2 * q + hh;               // 16-byte chunk within box h
+                        const uint32_t off = (uint32_t)(h * 16384 + e * 128 + ((cc ^ (e & 7)) << 4));
+                        *reinterpret_cast<uint4 *>(stage + off) =
+                            make_uint4(hw[4 * hh], hw[4 * hh + 1], hw[4 * hh + 2], hw[4 * hh + 3]);
+                    }
+                } else {
+                    if (jc < p.n) store16<D, OutT>(out, jc, 4 * h + q, v, sc);
+                }
+            }
+            if constexpr (TMA_OUT) {
+                fence_proxy_async_smem();
+                named_sync(3, kWsEpiThreads);
+                if (et == 0) {
+                    // Rows past n are clipped by the store.
+                    tma_store_2d(&omap, stage, 0, (int)(tile * kTileRows));
+                    tma_store_2d(&omap, stage + 16384, 64, (int)(tile * kTileRows));
+                    bulk_commit();
+                }
+            }
+            nu_c = nu_n;
+            row_n = row_nn;
+        }
+        if (TMA_OUT && et == 0) bulk_wait_all();         // stores complete before the CTA's memory goes away
+    } else if (lane == 0) {
+        const uint32_t pb_hi = smem_addr(sm + L::oPi), pb_lo = pb_hi + L::kPiPart;
+        uint32_t issued0 = 0u, issued1 = 0u;         // tiles issued into accumulator 0 and 1
+        ok = mbar_wait(bar_tab, 0);
+        for (int64_t i = 0; ok && first + i * gstride < ntiles; ++i) {
+            const int b = (int)(i & 1);
+            ok = mbar_wait(a_full + b, (uint32_t)((i >> 1) & 1));
+            // The read-back of tile i - 2 has left accumulator b.
+            if (ok && i >= 2) ok = mbar_wait(acc_empty + b, (uint32_t)(((i >> 1) - 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t ab = smem_addr(sm + L::oA + b * 2 * L::kATile);
+            issue_rotation<D>(tmem_base + (uint32_t)(b * D), ab, ab + L::kATile, pb_hi, pb_lo);
+            mma_commit(mma_done + b);
+            if (b) ++issued1;
+            else ++issued0;
+        }
+        // Every issued MMA has finished before the tensor memory is released.
+        if (issued0) mbar_wait(mma_done, (issued0 - 1u) & 1u, 1000000ull);
+        if (issued1) mbar_wait(mma_done + 1, (issued1 - 1u) & 1u, 1000000ull);
+    }
+    if (!ok) atomicOr(p.flags, (uint32_t)FQ_FLAG_TIMEOUT);
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWsMmaWarp) tmem_dealloc(tmem_base, L::kTmemCols);
+}
+
 template <int D, int K>
 constexpr int groups() { return D == 64 ? 4 : 2; }
 
@@ -351,8 +642,7 @@ constexpr bool lanes_possible() { return D == 64 && K <= 2; }
 
 template <int D, int K, int CBM, int BS, typename OutT>
 cudaError_t launch_dkm(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
-    constexpr int NG = groups<D, K>();
-    using L = DLayout<D, K, NG, CBM>;
+    constexpr int NG = D == 128 ? 1 : groups<D, K>();      // d = 128: one pipeline per CTA
     CUtensorMap omap;
     memset(&omap, 0, sizeof(omap));
     if (sizeof(OutT) == 2 && !encode_rows_tensor_map(&omap, p.out, p.n, D)) return cudaErrorInvalidValue;
@@ -361,15 +651,21 @@ cudaError_t launch_dkm(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
     if (grid > ctx->num_sms) grid = ctx->num_sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(NG * 128);
-    cfg.dynamicSmemBytes = L::kBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc<D, K, NG, CBM, BS, OutT>, omap, p);
+    if constexpr (D == 128) {
+        cfg.blockDim = dim3(kWsThreads);
+        cfg.dynamicSmemBytes = WsLayout::kBytes;
+        return cudaLaunchKernelEx(&cfg, decode_ws<K, BS, OutT>, omap, p);
+    } else {
+        cfg.blockDim = dim3(NG * 128);
+        cfg.dynamicSmemBytes = DLayout<D, K, NG, CBM>::kBytes;
+        return cudaLaunchKernelEx(&cfg, decode_tc<D, K, NG, CBM, BS, OutT>, omap, p);
+    }
 }
 
 template <int D, int K, int BS, typename OutT>
@@ -381,6 +677,14 @@ cudaError_t launch_dk(const fq_ctx *ctx, const DecParams &p, cudaStream_t s) {
 
 template <int D, int K, int CBM, int BS>
 cudaError_t prep_dkm() {
+    if constexpr (D == 128) {
+        static_assert(WsLayout::kBytes <= 227 * 1024, "shared memory budget");
+        cudaError_t e = cudaFuncSetAttribute(decode_ws<K, BS, __half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             WsLayout::kBytes);
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(decode_ws<K, BS, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    WsLayout::kBytes);
+    }
     constexpr int NG = groups<D, K>();
     using L = DLayout<D, K, NG, CBM>;
     static_assert(L::kBytes <= 227 * 1024, "shared memory budget");

@@ -18,7 +18,8 @@ def test_kernel_names_and_bytes():
     assert bench.kernel_of(synth.WORKLOADS[3], "encode") == "encode_k4_grid"
     assert bench.kernel_of(synth.WORKLOADS[4], "encode") == "encode_kq_tc"
     assert bench.kernel_of(synth.WORKLOADS[5], "encode") == "encode_full_tc"
-    assert bench.kernel_of(synth.WORKLOADS[4], "decode") == "decode_tc"
+    assert bench.kernel_of(synth.WORKLOADS[4], "decode") == "decode_ws"
+    assert bench.kernel_of(synth.WORKLOADS[2], "decode") == "decode_tc"
     enc, gat = bench.workload_bytes(synth.WORKLOADS[2], 256)
     assert enc == 2 * 64 + 4 + 32 and gat == 8 + 4 + 32 + 128
 

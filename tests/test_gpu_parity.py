@@ -146,6 +146,33 @@ def test_gather_out_of_range_rows_are_zero_and_flagged():
     parity.check_decode(out[ok], nu_d.cpu().numpy()[sel[ok]], idx[sel[ok]], C, Pi, fp16_output=False)
 
 
+@pytest.mark.parametrize("f32", [False, True])
+def test_d128_gather_many_tiles_per_cta_with_out_of_range_rows(f32):
+    # The d = 128 decoder pipelines consecutive tiles of a CTA through two A buffers and two
+    # accumulators: 152 x 6 tiles plus a ragged tail give every CTA six or seven tiles, so that
+    # every buffer is reused and every barrier phase wraps. Repeated and out-of-range indices mixed
+    # in; rows are checked against the oracle on a sample and out-of-range rows must be zero.
+    ctx, C, Pi = ctx_for(4)
+    M = 2000
+    x = synth.gaussian_rows(4, 9, M, 128, scale_spread=True)
+    nu_d, codes_d = gpu_encode(ctx, x)
+    assert fq.fq_status(ctx) == 0
+    n = 152 * 6 * 128 + 77
+    r = np.random.default_rng(5)
+    sel = r.integers(0, M, size=n)
+    bad = r.choice(n, size=300, replace=False)
+    sel[bad[:100]] = -1 - r.integers(0, 50, size=100)
+    sel[bad[100:]] = M + r.integers(0, 10 ** 9, size=200)
+    out = gpu_gather(ctx, nu_d, codes_d, M, sel, 128, f32=f32)
+    assert fq.fq_status(ctx) & fq.FQ_FLAG_RANGE
+    assert not out[bad].any()
+    idx_all = ofq.unpack(codes_d.cpu().numpy().view(np.uint32), M, 16, 12)
+    nu = nu_d.cpu().numpy()
+    good = np.setdiff1d(np.arange(n), bad)
+    pick = np.concatenate([good[:300], good[-300:], r.choice(good, size=1400, replace=False)])
+    parity.check_decode(out[pick], nu[sel[pick]], idx_all[sel[pick]], C, Pi, fp16_output=not f32)
+
+
 def _small_codebook(d, k, N, seed):
     from oracle import codebook as ocb
     r = np.random.default_rng(seed)

@@ -218,6 +218,25 @@ def test_records_at_any_bit_offset_preserve_neighbours(d, k, N, row0):
     ctx.close()
 
 
+@pytest.mark.parametrize("d,k,N", [(128, 1, 8), (128, 2, 256), (128, 4, 64), (128, 8, 128)])
+def test_d128_fp16_gather_with_run_time_field_widths(d, k, N):
+    # The d = 128 decoder's fp16 output path (staged rows, TMA box stores) for every k, with
+    # records whose fields are read at run time, over several tiles and a ragged tail.
+    C, Pi = _small_codebook(d, k, N, d * 7 + k * 3 + N)
+    ctx = fq.fq_codebook_load(C, Pi)
+    M = 1500
+    x = synth.gaussian_rows(7, 1, M, d, scale_spread=True)
+    nu_d, codes_d = gpu_encode(ctx, x)
+    sel = np.random.default_rng(k).integers(0, M, size=128 * 5 + 37)
+    got = gpu_gather(ctx, nu_d, codes_d, M, sel, d)
+    words = codes_d.cpu().numpy().view(np.uint32)
+    B = int(np.log2(N))
+    idx = np.array([ofq.record_indices(words, int(r), d // k, B) for r in sel])
+    parity.check_decode(got, nu_d.cpu().numpy()[sel], idx, C, Pi, fp16_output=True)
+    assert fq.fq_status(ctx) == 0
+    ctx.close()
+
+
 def test_append_matches_per_sequence_encode():
     ctx, C, Pi = ctx_for(4)
     n_seq, n_new, cap, t0 = 3, 50, 200, 17

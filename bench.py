@@ -671,8 +671,10 @@ def run_ours(args) -> None:
             "fp16_gbps": value * 2 * d / 1e9,
             "roofline": roofline,
             "cpu_baseline": cpu,
+            # The mean is the value; the spread shows how much of it the shared host link costs.
             "e2e": {"value": e2e_value, "unit": "vectors/s", "h2d_bytes_per_step": int(h2d),
-                    "d2h_bytes_per_step": int(d2h)},
+                    "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_total / args.steps,
+                    "median_ms_per_step": statistics.median(e2e_ms), "min_ms_per_step": min(e2e_ms)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "device_flags": flags,

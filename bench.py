@@ -406,6 +406,7 @@ def run_ours(args) -> None:
     G = int(idx_np.size)
     x_host = torch.from_numpy(x_np).pin_memory()
     i_host = torch.from_numpy(idx_np).pin_memory()
+    del x_np, idx_np                      # the pinned copies are the inputs from here on
     xs = x_host.to(dev)
     idx = i_host.to(dev)
     nu, codes = fq.alloc_store(ctx, MT, dev)

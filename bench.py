@@ -581,6 +581,7 @@ def run_ours(args) -> None:
     torch.cuda.synchronize(dev)
     if not (torch.equal(got[0], out.cpu()) and torch.equal(got[1], codes.cpu()) and torch.equal(got[2], nu.cpu())):
         raise SystemExit("the end-to-end pipeline returned other results than the device-resident step")
+    del got
     e2e_ms = []
     for _ in range(args.steps):
         flush.zero_()

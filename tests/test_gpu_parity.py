@@ -218,6 +218,21 @@ def test_records_at_any_bit_offset_preserve_neighbours(d, k, N, row0):
     ctx.close()
 
 
+@pytest.mark.parametrize("n", [1, 127, 129])
+@pytest.mark.parametrize("f32", [False, True])
+def test_d128_gather_of_few_rows(n, f32):
+    # One CTA (one tile: the second builder group has none) and one row either side of a tile.
+    ctx, C, Pi = ctx_for(4)
+    M = 300
+    x = synth.gaussian_rows(4, 10, M, 128, scale_spread=True)
+    nu_d, codes_d = gpu_encode(ctx, x)
+    sel = np.random.default_rng(n).integers(0, M, size=n)
+    got = gpu_gather(ctx, nu_d, codes_d, M, sel, 128, f32=f32)
+    idx = ofq.unpack(codes_d.cpu().numpy().view(np.uint32), M, 16, 12)
+    parity.check_decode(got, nu_d.cpu().numpy()[sel], idx[sel], C, Pi, fp16_output=not f32)
+    assert fq.fq_status(ctx) == 0
+
+
 @pytest.mark.parametrize("d,k,N", [(128, 1, 8), (128, 2, 256), (128, 4, 64), (128, 8, 128)])
 def test_d128_fp16_gather_with_run_time_field_widths(d, k, N):
     # The d = 128 decoder's fp16 output path (staged rows, TMA box stores) for every k, with

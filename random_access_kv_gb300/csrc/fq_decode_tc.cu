@@ -1,8 +1,10 @@
 // Tensor-core block decoder for k <= 8 [FibQuant §2.3, decoder], full and random-access
 // (gather, [FibQuant §1]: any vector decodes on its own from its fixed address).
 //
-// Per CTA: NG row groups of 128 threads, one thread per output vector (= TMEM lane), looping
-// over 128-row output tiles:
+// Each 128-row output tile goes through three steps. At d = 64 (decode_tc) a CTA runs NG row
+// groups of 128 threads, one thread per output vector (= TMEM lane), each group taking its tiles
+// through the steps in turn; at d = 128 (decode_ws, below) the steps of consecutive tiles run at
+// once in separate warps:
 //   1. Each thread reads its source row (idx[j] for a gather), its nu and its record, unpacks the
 //      d/k indices and writes the concatenated codewords y_hat, split into fp16 halves of
 //      2^10 y_hat (hi, lo), as row t of two shared-memory A operands (128-byte swizzle).

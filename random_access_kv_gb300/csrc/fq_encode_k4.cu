@@ -482,7 +482,7 @@ cudaError_t prepare_k4_grid(fq_ctx *ctx) {
     if (e != cudaSuccess) return e;
     Grid4 grid;
     build_grid4(C.data(), N, d, grid);
-    if (grid.F != kAxisF || grid.fo != kAxisF / 2 || grid.G > 32) return cudaErrorInvalidValue;
+    if (grid.F != kAxisF || grid.fo != kAxisF / 2 || grid.G > 40) return cudaErrorInvalidValue;
     ctx->k4_G = grid.G;
     ctx->k4_fs = grid.fs;
     std::vector<float> ncb(C.size());

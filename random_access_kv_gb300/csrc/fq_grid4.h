@@ -149,9 +149,10 @@ inline void build_grid4(const float *Cf, int N, int d, Grid4 &g) {
         }
         cc[n] = s;
     }
-    // Coarse resolution: about 32 cells per axis for 1024 codewords, scaled with N^(1/4).
-    g.G = (int)lround(32.0 * pow(N / 1024.0, 0.25));
-    g.G = std::min(32, std::max(4, g.G));
+    // Coarse resolution: about 40 cells per axis for 1024 codewords, scaled with N^(1/4), at most
+    // 40 (an 82 MB table of 32-byte records, which stays in L2 beside the streamed input).
+    g.G = (int)lround(40.0 * pow(N / 1024.0, 0.25));
+    g.G = std::min(40, std::max(4, g.G));
     const int G = g.G, F = g.F, fo = g.fo;
     // Extent: the codebook's, or 4.9 standard deviations of a coordinate (1 / sqrt d).
     const double R = fmax(1.05 * cmax, 4.9 / sqrt((double)d));
